@@ -1,0 +1,144 @@
+/*
+ * dualkv.h -- C ABI of libdualkv.so: DualKV shared-prompt exact attention,
+ * forward and backward, on one NVIDIA GB300 (sm_103a).
+ *
+ * Source of the method: "DualKV: Shared-Prompt Flash Attention for Efficient
+ * RL Training with Large Rollouts and Long Contexts", abstract.  A micro-batch
+ * holds one shared prompt of P tokens and N response segments; the data
+ * pipeline packs the N(P+R) replicated tokens into P + sum_n R_n rows, and
+ * the fused forward and backward kernels walk two disjoint KV regions (the
+ * shared prompt and the query's own segment) in one launch.  The result is
+ * stated to equal standard causal attention on the N replicated sequences.
+ *
+ * Packed layout (all buffers contiguous, device memory unless stated):
+ *   row t in [0, P)                 prompt token t, position t
+ *   row P + R_offsets[n] + r        response token r of segment n, position P + r
+ *   T = P + R_offsets[N] rows in total.
+ *   q, out, dout, dq : [T, Hq, D]  bf16
+ *   k, v, dk, dv     : [T, Hkv, D] bf16
+ *   lse              : [Hq, T]     fp32, natural-log log-sum-exp of each row
+ * Attention rule for a query at position p and a key at position p':
+ *   the key lies in the prompt or in the query's own segment, p' <= p, and
+ *   (window <= 0 or p - p' < window).
+ * GQA: q-head h reads kv-head h / (Hq / Hkv).
+ *
+ * Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL is
+ * the legacy default stream).  Outputs are fully overwritten, never
+ * accumulated.  Results are bitwise deterministic for a given GPU, library
+ * build and input.  Inputs must be finite.  Every device pointer must be
+ * 16-byte aligned.  The caller owns every buffer it passes; the library owns
+ * only a per-layout plan cache (small device arrays) and a per-device status
+ * word, both freed by dualkv_release().
+ *
+ * Return codes: DUALKV_OK, or one of the DUALKV_ERR_* values below; on an
+ * error nothing is launched (except DUALKV_ERR_CUDA, which reports a failed
+ * launch).  Kernel-side failures (a bounded wait that timed out, an index
+ * out of range) do not abort the launch: they are recorded in the status
+ * word and reported by dualkv_check_status().
+ */
+#ifndef DUALKV_H_
+#define DUALKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DUALKV_OK 0
+#define DUALKV_ERR_INVALID 1     /* bad sizes, offsets, head counts or head dimension */
+#define DUALKV_ERR_ALIGN 2       /* a device pointer is not 16-byte aligned */
+#define DUALKV_ERR_WORKSPACE 3   /* workspace missing or smaller than dualkv_bwd_workspace_bytes() */
+#define DUALKV_ERR_CUDA 4        /* a CUDA runtime call or kernel launch failed */
+#define DUALKV_ERR_DEVICE 5      /* a kernel reported a timeout or bounds violation */
+#define DUALKV_ERR_UNSUPPORTED 6 /* valid arguments outside what this build supports */
+
+/*
+ * Forward pass (paper abstract: "fused CUDA forward ... kernels that iterate
+ * over two disjoint KV regions -- shared context and per-sequence response --
+ * in a single kernel launch").  For every packed query row and q-head:
+ * S = scale * q k^T over the allowed keys of the prompt region and then of the
+ * row's own segment, online softmax, out = softmax(S) v, lse = log-sum-exp(S).
+ *
+ *   q, k, v        device, bf16, layouts above (read only)
+ *   P >= 0         prompt tokens; N >= 1 segments
+ *   R_offsets      HOST int32[N+1], R_offsets[0] = 0, non-decreasing;
+ *                  segment n has R_offsets[n+1] - R_offsets[n] >= 0 tokens
+ *   Hq, Hkv        Hq % Hkv == 0
+ *   D              head dimension: 64 or 128 (512: DUALKV_ERR_UNSUPPORTED in this build)
+ *   scale          softmax scale (typically 1/sqrt(D))
+ *   window         <= 0: global causal; else sliding window of `window` keys
+ *   out            device bf16 [T, Hq, D] (written)
+ *   lse            device fp32 [Hq, T] (written)
+ */
+int dualkv_fwd(const void* q, const void* k, const void* v, int P, int N, const int32_t* R_offsets, int Hq,
+               int Hkv, int D, float scale, int window, void* out, float* lse, void* stream);
+
+/*
+ * Bytes of device workspace dualkv_bwd needs for this layout: the per-row
+ * rowsum(dO * O) and log2-scaled LSE (2 * Hq * T fp32) plus the fp32 partial
+ * dK/dV tiles of prompt key tiles whose query walk is split across CTAs.
+ * Returns 0 when the arguments are invalid.
+ */
+size_t dualkv_bwd_workspace_bytes(int P, int N, const int32_t* R_offsets, int Hq, int Hkv, int D, int window);
+
+/*
+ * Backward pass (paper abstract: fused backward kernels; the prompt's dK/dV
+ * gather the contributions of every segment, since the packed result equals
+ * standard attention on the replicated sequences with prompt gradients summed).
+ * Runs: preprocess (Delta = rowsum(dout * out)), dK/dV (each key tile walks
+ * every query block that attends it in a fixed order: group heads ascending,
+ * prompt query blocks ascending, then segments 0..N-1 ascending), a
+ * fixed-order reduction of split prompt tiles, and dQ.
+ *
+ *   q, k, v, out, lse, dout   as produced for/by dualkv_fwd with the same layout
+ *   dq, dk, dv                device bf16, written
+ *   workspace                 device, >= dualkv_bwd_workspace_bytes(), 256-byte aligned
+ */
+int dualkv_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout,
+               int P, int N, const int32_t* R_offsets, int Hq, int Hkv, int D, float scale, int window, void* dq,
+               void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Packing indices (host only, no GPU needed; paper abstract: the pipeline
+ * "repacks N(P+R) tokens into P+NR tokens").  All outputs are HOST int32:
+ *   seg_id[T]          -1 for prompt rows, else the segment of the row
+ *   pos_id[T]          position of the row in its replicated sequence
+ *   cu_seqlens_rep[N+1] start of replicated sequence n (length P + R_n)
+ *   rep2pack[sum_n (P+R_n)]  packed row of each replicated row
+ * Any output pointer may be NULL.  Returns DUALKV_OK or DUALKV_ERR_INVALID.
+ */
+int dualkv_build_index(int P, int N, const int32_t* R_offsets, int32_t* seg_id, int32_t* pos_id,
+                       int32_t* cu_seqlens_rep, int32_t* rep2pack);
+
+/*
+ * Token-reduction factor rho = sum_n (P + R_n) / (P + sum_n R_n) (paper
+ * abstract: rho = N(P+R)/(P+NR) for equal lengths).  Host only; -1 on invalid input.
+ */
+double dualkv_rho(int P, int N, const int32_t* R_offsets);
+
+/*
+ * Attended (query, key) pairs of one head in the packed layout, each packed
+ * query row counted once.  Host only; -1 on invalid input.
+ */
+int64_t dualkv_pairs(int P, int N, const int32_t* R_offsets, int window);
+
+/*
+ * Synchronises `stream`, reads and clears the status word of the current
+ * device, and returns DUALKV_OK or DUALKV_ERR_DEVICE (a kernel timed out in
+ * a bounded wait or found an index out of range) or DUALKV_ERR_CUDA.
+ */
+int dualkv_check_status(void* stream);
+
+/* Static, NUL-terminated description of a return code. */
+const char* dualkv_error_string(int code);
+
+/* Frees the plan cache and status words.  Not safe while launches are pending. */
+void dualkv_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DUALKV_H_ */

@@ -1,0 +1,339 @@
+// api.cu -- the C ABI of libdualkv.so (declared in include/dualkv.h): argument
+// validation, the per-layout plan cache, TMA tensor maps, the per-device status
+// word and the launch sequence of the forward and backward passes.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <memory>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/dualkv.h"
+#include "kernels.h"
+#include "plan.h"
+
+using namespace dkv;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+std::mutex g_mu;
+EncodeTiledFn g_encode = nullptr;
+std::map<int, uint32_t*> g_status;  // device -> status word
+
+// dK/dV key tiles whose query walk is longer than this many query blocks are
+// split into contiguous chunks reduced in a fixed order.
+constexpr int kMaxDkvIters = 512;
+
+struct DevPlan {
+  int device = -1;
+  bool fwd_ready = false, bwd_ready = false;
+  QTileItem* fwd_items = nullptr;
+  int n_fwd = 0;
+  QTileItem* dq_items = nullptr;
+  int n_dq = 0;
+  KVTileItem* kv_items = nullptr;
+  int n_kv = 0;
+  QBlock* qblocks = nullptr;
+  ReduceItem* reduces = nullptr;
+  int n_reduce = 0;
+  int nslots = 0;
+  ~DevPlan() {
+    cudaFree(fwd_items);
+    cudaFree(dq_items);
+    cudaFree(kv_items);
+    cudaFree(qblocks);
+    cudaFree(reduces);
+  }
+};
+std::map<std::string, std::unique_ptr<DevPlan>> g_plans;
+
+std::string plan_key(int device, int P, int N, const int32_t* off, int Hq, int Hkv, int D, int window) {
+  std::string k;
+  k.reserve(64 + 4 * (N + 1));
+  int32_t hdr[7] = {device, P, N, Hq, Hkv, D, window <= 0 ? 0 : window};
+  k.append(reinterpret_cast<const char*>(hdr), sizeof(hdr));
+  k.append(reinterpret_cast<const char*>(off), sizeof(int32_t) * (N + 1));
+  return k;
+}
+
+template <typename T>
+cudaError_t upload(T** dst, const std::vector<T>& v) {
+  *dst = nullptr;
+  if (v.empty()) return cudaSuccess;
+  cudaError_t e = cudaMalloc(dst, sizeof(T) * v.size());
+  if (e != cudaSuccess) return e;
+  return cudaMemcpy(*dst, v.data(), sizeof(T) * v.size(), cudaMemcpyHostToDevice);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int ensure_encode() {
+  if (g_encode) return DUALKV_OK;
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return DUALKV_ERR_CUDA;
+  g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  return DUALKV_OK;
+}
+
+int status_word(int device, uint32_t** out) {
+  auto it = g_status.find(device);
+  if (it != g_status.end()) {
+    *out = it->second;
+    return DUALKV_OK;
+  }
+  uint32_t* p = nullptr;
+  if (cudaMalloc(&p, 256) != cudaSuccess) return DUALKV_ERR_CUDA;
+  if (cudaMemset(p, 0, 256) != cudaSuccess) return DUALKV_ERR_CUDA;
+  g_status[device] = p;
+  *out = p;
+  return DUALKV_OK;
+}
+
+// [T, H, D] bf16 rows, box of 64 head-dim columns x 1 head x box_rows rows, 128-byte swizzle.
+int make_tmap(CUtensorMap* m, const void* base, int64_t T, int H, int D, int box_rows) {
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DUALKV_OK : DUALKV_ERR_CUDA;
+}
+
+// Looks up (or builds) the plan of a layout; caller holds g_mu.
+int get_plan(int P, int N, const int32_t* off, int Hq, int Hkv, int D, int window, bool need_bwd, DevPlan** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DUALKV_ERR_CUDA;
+  const std::string key = plan_key(dev, P, N, off, Hq, Hkv, D, window);
+  auto& slot = g_plans[key];
+  if (!slot) {
+    slot.reset(new DevPlan());
+    slot->device = dev;
+  }
+  DevPlan* pl = slot.get();
+  Layout L{P, N, std::vector<int32_t>(off, off + N + 1), Hq, Hkv, D, window <= 0 ? 0 : window};
+  if (!pl->fwd_ready) {
+    auto items = plan_qtiles(L, fwd_query_tile(D), fwd_key_tile(D));
+    if (upload(&pl->fwd_items, items) != cudaSuccess) return DUALKV_ERR_CUDA;
+    pl->n_fwd = (int)items.size();
+    pl->fwd_ready = true;
+  }
+  if (need_bwd && !pl->bwd_ready) {
+    auto dq = plan_qtiles(L, dq_query_tile(D), dq_key_tile(D));
+    if (upload(&pl->dq_items, dq) != cudaSuccess) return DUALKV_ERR_CUDA;
+    pl->n_dq = (int)dq.size();
+    KVPlan kv = plan_kvtiles(L, dkv_key_tile(D), dkv_query_block(D), kMaxDkvIters);
+    if (upload(&pl->kv_items, kv.items) != cudaSuccess) return DUALKV_ERR_CUDA;
+    if (upload(&pl->qblocks, kv.qblocks) != cudaSuccess) return DUALKV_ERR_CUDA;
+    if (upload(&pl->reduces, kv.reduces) != cudaSuccess) return DUALKV_ERR_CUDA;
+    pl->n_kv = (int)kv.items.size();
+    pl->n_reduce = (int)kv.reduces.size();
+    pl->nslots = kv.nslots;
+    pl->bwd_ready = true;
+  }
+  *out = pl;
+  return DUALKV_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct WsLayout {
+  size_t delta, lse2, partial, total;
+};
+WsLayout ws_layout(int64_t T, int Hq, int D, int nslots) {
+  WsLayout w;
+  w.delta = 0;
+  w.lse2 = align256(sizeof(float) * (size_t)Hq * T);
+  w.partial = w.lse2 + align256(sizeof(float) * (size_t)Hq * T);
+  w.total = w.partial + sizeof(float) * (size_t)nslots * 2 * dkv_key_tile(D) * D;
+  return w;
+}
+
+bool supported_d(int D) { return D == 64 || D == 128; }
+
+}  // namespace
+
+extern "C" {
+
+int dualkv_fwd(const void* q, const void* k, const void* v, int P, int N, const int32_t* R_offsets, int Hq, int Hkv,
+               int D, float scale, int window, void* out, float* lse, void* stream) {
+  if (validate_layout(P, N, R_offsets, Hq, Hkv, D)) return DUALKV_ERR_INVALID;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return DUALKV_ERR_INVALID;
+  if (!q || !k || !v || !out || !lse) return DUALKV_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse)) return DUALKV_ERR_ALIGN;
+  if (!supported_d(D)) return DUALKV_ERR_UNSUPPORTED;
+  const int64_t T = (int64_t)P + R_offsets[N];
+  std::lock_guard<std::mutex> lock(g_mu);
+  int rc = ensure_encode();
+  if (rc) return rc;
+  DevPlan* pl = nullptr;
+  if ((rc = get_plan(P, N, R_offsets, Hq, Hkv, D, window, false, &pl))) return rc;
+  uint32_t* status = nullptr;
+  if ((rc = status_word(pl->device, &status))) return rc;
+  CUtensorMap tq, tk, tv;
+  if (make_tmap(&tq, q, T, Hq, D, fwd_query_tile(D)) || make_tmap(&tk, k, T, Hkv, D, fwd_key_tile(D)) ||
+      make_tmap(&tv, v, T, Hkv, D, fwd_key_tile(D)))
+    return DUALKV_ERR_CUDA;
+  FwdArgs a{pl->fwd_items, static_cast<__nv_bfloat16*>(out), lse, (int)T, Hq, Hkv, window <= 0 ? 0 : window,
+            scale * 1.4426950408889634f, status};
+  if (launch_fwd(D, tq, tk, tv, a, pl->n_fwd, static_cast<cudaStream_t>(stream)) != cudaSuccess) return DUALKV_ERR_CUDA;
+  return DUALKV_OK;
+}
+
+size_t dualkv_bwd_workspace_bytes(int P, int N, const int32_t* R_offsets, int Hq, int Hkv, int D, int window) {
+  if (validate_layout(P, N, R_offsets, Hq, Hkv, D) || !supported_d(D)) return 0;
+  Layout L{P, N, std::vector<int32_t>(R_offsets, R_offsets + N + 1), Hq, Hkv, D, window <= 0 ? 0 : window};
+  KVPlan kv = plan_kvtiles(L, dkv_key_tile(D), dkv_query_block(D), kMaxDkvIters);
+  return ws_layout(L.T(), Hq, D, kv.nslots).total;
+}
+
+int dualkv_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout, int P,
+               int N, const int32_t* R_offsets, int Hq, int Hkv, int D, float scale, int window, void* dq, void* dk,
+               void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  if (validate_layout(P, N, R_offsets, Hq, Hkv, D)) return DUALKV_ERR_INVALID;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return DUALKV_ERR_INVALID;
+  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return DUALKV_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return DUALKV_ERR_ALIGN;
+  if (!supported_d(D)) return DUALKV_ERR_UNSUPPORTED;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return DUALKV_ERR_WORKSPACE;
+  const int64_t T = (int64_t)P + R_offsets[N];
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_mu);
+  int rc = ensure_encode();
+  if (rc) return rc;
+  DevPlan* pl = nullptr;
+  if ((rc = get_plan(P, N, R_offsets, Hq, Hkv, D, window, true, &pl))) return rc;
+  const WsLayout ws = ws_layout(T, Hq, D, pl->nslots);
+  if (workspace_bytes < ws.total) return DUALKV_ERR_WORKSPACE;
+  uint32_t* status = nullptr;
+  if ((rc = status_word(pl->device, &status))) return rc;
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  float* delta = reinterpret_cast<float*>(wsb + ws.delta);
+  float* lse2 = reinterpret_cast<float*>(wsb + ws.lse2);
+  float* partial = reinterpret_cast<float*>(wsb + ws.partial);
+  const int W = window <= 0 ? 0 : window;
+  const float sl2 = scale * 1.4426950408889634f;
+
+  PrepArgs pa{static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, delta, lse2, T, Hq, D};
+  if (launch_prep(pa, st) != cudaSuccess) return DUALKV_ERR_CUDA;
+
+  CUtensorMap tq, tk, tv, tdo;
+  if (make_tmap(&tq, q, T, Hq, D, dkv_query_block(D)) || make_tmap(&tk, k, T, Hkv, D, dkv_key_tile(D)) ||
+      make_tmap(&tv, v, T, Hkv, D, dkv_key_tile(D)) || make_tmap(&tdo, dout, T, Hq, D, dkv_query_block(D)))
+    return DUALKV_ERR_CUDA;
+  DkvArgs ka{pl->kv_items, pl->qblocks, delta, lse2, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
+             partial, (int)T, Hq, Hkv, W, sl2, scale, status};
+  if (launch_dkv(D, tq, tk, tv, tdo, ka, pl->n_kv, st) != cudaSuccess) return DUALKV_ERR_CUDA;
+  if (pl->n_reduce > 0) {
+    ReduceArgs ra{pl->reduces, partial, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), Hkv, D,
+                  dkv_key_tile(D)};
+    if (launch_reduce(ra, pl->n_reduce, st) != cudaSuccess) return DUALKV_ERR_CUDA;
+  }
+
+  CUtensorMap tq2, tk2, tv2, tdo2;
+  if (make_tmap(&tq2, q, T, Hq, D, dq_query_tile(D)) || make_tmap(&tk2, k, T, Hkv, D, dq_key_tile(D)) ||
+      make_tmap(&tv2, v, T, Hkv, D, dq_key_tile(D)) || make_tmap(&tdo2, dout, T, Hq, D, dq_query_tile(D)))
+    return DUALKV_ERR_CUDA;
+  DqArgs qa{pl->dq_items, delta, lse2, static_cast<__nv_bfloat16*>(dq), (int)T, Hq, Hkv, W, sl2, scale, status};
+  if (launch_dq(D, tq2, tk2, tv2, tdo2, qa, pl->n_dq, st) != cudaSuccess) return DUALKV_ERR_CUDA;
+  return DUALKV_OK;
+}
+
+int dualkv_build_index(int P, int N, const int32_t* R_offsets, int32_t* seg_id, int32_t* pos_id,
+                       int32_t* cu_seqlens_rep, int32_t* rep2pack) {
+  if (P < 0 || N < 1 || !R_offsets || R_offsets[0] != 0) return DUALKV_ERR_INVALID;
+  for (int n = 0; n < N; ++n)
+    if (R_offsets[n + 1] < R_offsets[n]) return DUALKV_ERR_INVALID;
+  if ((int64_t)N * P + R_offsets[N] > INT32_MAX) return DUALKV_ERR_INVALID;
+  build_index(P, N, R_offsets, seg_id, pos_id, cu_seqlens_rep, rep2pack);
+  return DUALKV_OK;
+}
+
+double dualkv_rho(int P, int N, const int32_t* R_offsets) {
+  if (P < 0 || N < 1 || !R_offsets || R_offsets[0] != 0) return -1.0;
+  for (int n = 0; n < N; ++n)
+    if (R_offsets[n + 1] < R_offsets[n]) return -1.0;
+  const double packed = (double)P + R_offsets[N];
+  if (packed <= 0) return -1.0;
+  return ((double)N * P + R_offsets[N]) / packed;
+}
+
+int64_t dualkv_pairs(int P, int N, const int32_t* R_offsets, int window) {
+  if (P < 0 || N < 1 || !R_offsets || R_offsets[0] != 0) return -1;
+  for (int n = 0; n < N; ++n)
+    if (R_offsets[n + 1] < R_offsets[n]) return -1;
+  // keys attended by the query at position p: p + 1, or min(p + 1, window)
+  auto upto = [window](int64_t len) -> int64_t {  // sum over positions 0..len-1
+    if (window <= 0 || window >= len) return len * (len + 1) / 2;
+    const int64_t w = window;
+    return w * (w + 1) / 2 + (len - w) * w;
+  };
+  int64_t total = upto(P);
+  for (int n = 0; n < N; ++n) {
+    const int64_t R = R_offsets[n + 1] - R_offsets[n];
+    total += upto((int64_t)P + R) - upto(P);
+  }
+  return total;
+}
+
+int dualkv_check_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DUALKV_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DUALKV_ERR_CUDA;
+  uint32_t* st = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (status_word(dev, &st)) return DUALKV_ERR_CUDA;
+  }
+  uint32_t h = 0;
+  if (cudaMemcpy(&h, st, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return DUALKV_ERR_CUDA;
+  if (h) {
+    cudaMemset(st, 0, sizeof(uint32_t));
+    return DUALKV_ERR_DEVICE;
+  }
+  return DUALKV_OK;
+}
+
+const char* dualkv_error_string(int code) {
+  switch (code) {
+    case DUALKV_OK:
+      return "ok";
+    case DUALKV_ERR_INVALID:
+      return "invalid argument (sizes, offsets, head counts, head dimension or scale)";
+    case DUALKV_ERR_ALIGN:
+      return "a device pointer is not 16-byte aligned";
+    case DUALKV_ERR_WORKSPACE:
+      return "workspace missing, misaligned or too small";
+    case DUALKV_ERR_CUDA:
+      return "a CUDA runtime call or kernel launch failed";
+    case DUALKV_ERR_DEVICE:
+      return "a kernel reported a timed-out wait or an index out of range";
+    case DUALKV_ERR_UNSUPPORTED:
+      return "valid arguments outside what this build supports";
+    default:
+      return "unknown error code";
+  }
+}
+
+void dualkv_release(void) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_plans.clear();
+  for (auto& kv : g_status) cudaFree(kv.second);
+  g_status.clear();
+}
+
+}  // extern "C"

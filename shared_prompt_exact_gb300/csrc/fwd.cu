@@ -1,0 +1,380 @@
+// fwd.cu -- DualKV forward kernel for sm_103a (head dimension 64 / 128).
+//
+// DualKV paper, abstract: a fused forward kernel that iterates over two
+// disjoint KV regions -- the shared prompt and the query's own response
+// segment -- in a single launch.  One CTA takes one query tile (128 packed
+// rows of one region) of one q-head and walks the key tiles of region 0
+// (prompt) and then region 1 (own segment), clipped to the causal / window
+// range, with an online softmax.
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer: Q tile once, then K and V tiles into a ring, in
+//               the order the MMA warp consumes them (K0, K1, V0, K2, V1, ...)
+//   warp 1      TMEM owner and MMA issuer (one thread): S_j = Q K_j^T into one
+//               of two TMEM S buffers, O += P_{j-1} V_{j-1} into the TMEM O
+//               accumulator
+//   warps 2-5   softmax: thread <-> query row (TMEM lane); reads S_j, masks,
+//               keeps the running max m and sum l, writes P_j (bf16) to shared
+//               memory, rescales O in TMEM when m grows by more than 2^8, and
+//               finally writes out = O / l and lse = m + ln l.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dkv {
+
+namespace {
+
+template <int D>
+struct FwdCfg {
+  static constexpr int BM = 128, BN = 128;
+  static constexpr int KCH = D / 64;                  // 64-column chunks of the head dimension
+  static constexpr int Q_BYTES = BM * D * 2;
+  static constexpr int TILE_BYTES = BN * D * 2;        // one K or V tile
+  static constexpr int P_BYTES = BM * BN * 2;
+  static constexpr int NST = (D == 128) ? 4 : 6;       // ring slots
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_P = OFF_Q + Q_BYTES;
+  static constexpr int OFF_RING = OFF_P + 2 * P_BYTES;
+  static constexpr int SMEM_BYTES = OFF_RING + NST * TILE_BYTES + 1024;  // + alignment slack
+  static constexpr uint32_t TM_S = 0;                  // S buffers at columns 0 and BN
+  static constexpr uint32_t TM_O = 2 * BN;             // O accumulator
+  static constexpr uint32_t TM_COLS = 512;
+  static constexpr float RESCALE_THRESHOLD = 8.0f;     // log2 units
+};
+
+struct FwdSmemCtl {
+  uint64_t q_full;
+  uint64_t ring_full[8], ring_empty[8];
+  uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ void tile_of(const QTileItem& it, int j, int& r, int& t) {
+  const int n0 = it.reg[0].t_hi - it.reg[0].t_lo;
+  if (j < n0) {
+    r = 0;
+    t = it.reg[0].t_lo + j;
+  } else {
+    r = 1;
+    t = it.reg[1].t_lo + (j - n0);
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ FwdSmemCtl ctl;
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sP = smem + C::OFF_P;
+  uint8_t* sRing = smem + C::OFF_RING;
+
+  const QTileItem it = a.items[blockIdx.x];
+  const int nt0 = it.reg[0].t_hi - it.reg[0].t_lo;
+  const int nt = nt0 + (it.reg[1].t_hi - it.reg[1].t_lo);
+  const int kvh = it.head / (a.Hq / a.Hkv);
+  const uint32_t warp = warp_id(), lane = lane_id();
+  FailState fs{&ctl.abort_flag, a.status};
+
+  if (threadIdx.x == 0) {
+    ctl.abort_flag = 0;
+    mbar_init(&ctl.q_full, 1);
+    for (int i = 0; i < C::NST; ++i) {
+      mbar_init(&ctl.ring_full[i], 1);
+      mbar_init(&ctl.ring_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl.s_full[i], 1);
+      mbar_init(&ctl.s_empty[i], 4);
+      mbar_init(&ctl.p_full[i], 4);
+      mbar_init(&ctl.pv_done[i], 1);
+    }
+    mbar_init(&ctl.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl.tmem_base, C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && nt > 0) {
+      tma_prefetch_desc(&tmQ);
+      tma_prefetch_desc(&tmK);
+      tma_prefetch_desc(&tmV);
+      mbar_arrive_expect_tx(&ctl.q_full, C::Q_BYTES);
+      for (int c = 0; c < C::KCH; ++c)
+        tma_load_3d(sQ + c * C::BM * 128, &tmQ, &ctl.q_full, c * 64, it.head, it.q_row0);
+      int slot = 0;
+      uint32_t phase = 0;
+      int pushes = 0;
+      bool ok = true;
+      for (int j = 0; j <= nt && ok; ++j) {
+        for (int kind = 0; kind < 2 && ok; ++kind) {
+          const int jj = kind == 0 ? j : j - 1;  // K_j then V_{j-1}
+          if (jj < 0 || jj >= nt) continue;
+          int r, t;
+          tile_of(it, jj, r, t);
+          const int key_row = it.reg[r].row0 + t * C::BN;
+          if (!mbar_wait(&ctl.ring_empty[slot], phase ^ 1, fs)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&ctl.ring_full[slot], C::TILE_BYTES);
+          uint8_t* dst = sRing + slot * C::TILE_BYTES;
+          const CUtensorMap* tm = kind == 0 ? &tmK : &tmV;
+          for (int c = 0; c < C::KCH; ++c) tma_load_3d(dst + c * C::BN * 128, tm, &ctl.ring_full[slot], c * 64, kvh, key_row);
+          ++pushes;
+          if (++slot == C::NST) {
+            slot = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // drain: wait for every copy still in flight before the CTA can exit
+        mbar_wait_drain(&ctl.q_full, 0, kWaitLimitNs);
+        for (int back = 1; back <= C::NST && back <= pushes; ++back) {
+          int s = slot - back;
+          uint32_t ph = phase;
+          if (s < 0) {
+            s += C::NST;
+            ph ^= 1;
+          }
+          mbar_wait_drain(&ctl.ring_full[s], ph, kWaitLimitNs);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && nt > 0) {
+      constexpr uint32_t idS = idesc_bf16(128, C::BN, 0, 0);
+      constexpr uint32_t idO = idesc_bf16(128, D, 0, 1);
+      const uint32_t aQ = smem_u32(sQ), aP = smem_u32(sP), aRing = smem_u32(sRing);
+      int slot = 0;
+      uint32_t phase = 0;
+      bool ok = mbar_wait(&ctl.q_full, 0, fs);
+      tc_fence_after();
+      for (int j = 0; j <= nt && ok; ++j) {
+        if (j < nt) {
+          const int b = j & 1;
+          if (!(ok = mbar_wait(&ctl.s_empty[b], ((j >> 1) & 1) ^ 1, fs))) break;
+          if (!(ok = mbar_wait(&ctl.ring_full[slot], phase, fs))) break;
+          tc_fence_after();
+          const uint32_t kbase = aRing + slot * C::TILE_BYTES;
+#pragma unroll
+          for (int c = 0; c < C::KCH; ++c)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = sdesc_sw128(aQ + c * C::BM * 128 + k * 32, 16, 1024);
+              const uint64_t bd = sdesc_sw128(kbase + c * C::BN * 128 + k * 32, 16, 1024);
+              mma_bf16_ss(tmem + C::TM_S + b * C::BN, ad, bd, idS, (c | k) != 0);
+            }
+          mma_commit(&ctl.ring_empty[slot]);
+          mma_commit(&ctl.s_full[b]);
+          if (++slot == C::NST) {
+            slot = 0;
+            phase ^= 1;
+          }
+        }
+        if (j >= 1) {
+          const int jj = j - 1, b = jj & 1;
+          if (!(ok = mbar_wait(&ctl.p_full[b], (jj >> 1) & 1, fs))) break;
+          if (!(ok = mbar_wait(&ctl.ring_full[slot], phase, fs))) break;
+          tc_fence_after();
+          const uint32_t vbase = aRing + slot * C::TILE_BYTES;
+          const uint32_t pbase = aP + b * C::P_BYTES;
+#pragma unroll
+          for (int k = 0; k < C::BN / 16; ++k) {
+            const uint64_t ad = sdesc_sw128(pbase + (k >> 2) * C::BM * 128 + (k & 3) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(vbase + k * 16 * 128, C::BN * 128, 1024);
+            mma_bf16_ss(tmem + C::TM_O, ad, bd, idO, (jj > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(&ctl.ring_empty[slot]);
+          mma_commit(&ctl.pv_done[b]);
+          if (++slot == C::NST) {
+            slot = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // every MMA issued above must finish before TMEM is released
+      mma_commit(&ctl.drain);
+      mbar_wait_drain(&ctl.drain, 0, kWaitLimitNs);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const uint32_t wq = warp & 3;
+    const int row = (int)(wq * 32 + lane);
+    const uint32_t tl = tmem + ((wq * 32) << 16);
+    const int qpos = it.q_pos0 + row;
+    const float sl2 = a.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      const int b = j & 1;
+      if (!(ok = mbar_wait(&ctl.s_full[b], (j >> 1) & 1, fs))) break;
+      tc_fence_after();
+      int r, t;
+      tile_of(it, j, r, t);
+      const KeyRegion& kr = it.reg[r];
+      const int kl0 = t * C::BN;  // local index of the tile's first key in its region
+      int lo = 0;
+      if (a.window > 0) lo = max(0, qpos - a.window + 1 - kr.pos0);
+      const int hi = min(kr.count - 1, qpos - kr.pos0);
+      const int clo = lo - kl0, chi = hi - kl0;  // allowed columns [clo, chi]
+      const bool full = (clo <= 0) && (chi >= C::BN - 1);
+
+      float s[C::BN];
+#pragma unroll
+      for (int c4 = 0; c4 < C::BN / 32; ++c4) {
+        uint32_t rr[32];
+        tmem_ld32(tl + C::TM_S + b * C::BN + c4 * 32, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c4 * 32 + i] = __uint_as_float(rr[i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.s_empty[b]);
+
+      float mx = -INFINITY;
+      if (full) {
+#pragma unroll
+        for (int c = 0; c < C::BN; ++c) mx = fmaxf(mx, s[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < C::BN; ++c) {
+          s[c] = (c < clo || c > chi) ? -INFINITY : s[c];
+          mx = fmaxf(mx, s[c]);
+        }
+      }
+      const float m_tile = mx * sl2;  // -inf stays -inf (sl2 > 0)
+      const float m_new = fmaxf(m, m_tile);
+      if (j == 0) {
+        m = m_new;
+      } else if (__any_sync(0xffffffffu, m_new > m + C::RESCALE_THRESHOLD)) {
+        const float alpha = ex2_approx(m - m_new);  // m = -inf gives 0; O and l are 0 then
+        if (!(ok = mbar_wait(&ctl.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, fs))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c4 = 0; c4 < D / 32; ++c4) {
+          uint32_t rr[32];
+          tmem_ld32(tl + C::TM_O + c4 * 32, rr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+          tmem_st32(tl + C::TM_O + c4 * 32, rr);
+        }
+        tmem_st_wait();
+        l *= alpha;
+        m = m_new;
+      }
+      const float m_use = (m == -INFINITY) ? 0.f : m;
+      // the P buffer is free once PV_{j-2} has completed
+      if (j >= 2 && !(ok = mbar_wait(&ctl.pv_done[b], ((j - 2) >> 1) & 1, fs))) break;
+      const uint32_t pb = smem_u32(sP + b * C::P_BYTES);
+      float sum = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < C::BN / 64; ++ch)
+#pragma unroll
+        for (int pc = 0; pc < 8; ++pc) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = ch * 64 + pc * 8 + e * 2;
+            const float p0 = ex2_approx(fmaf(s[c], sl2, -m_use));
+            const float p1 = ex2_approx(fmaf(s[c + 1], sl2, -m_use));
+            sum += p0 + p1;
+            w[e] = pack_bf16x2(p0, p1);
+          }
+          st_shared_v4(pb + ch * C::BM * 128 + sw128_offset(row, pc), w[0], w[1], w[2], w[3]);
+        }
+      l += sum;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.p_full[b]);
+    }
+    if (ok && nt > 0) {
+      // epilogue: out = O / l, lse = (m + log2 l) ln 2
+      ok = mbar_wait(&ctl.pv_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, fs);
+      tc_fence_after();
+      if (ok) {
+        const bool valid = row < it.q_rows;
+        const float inv_l = 1.f / l;
+        __nv_bfloat16* orow = a.out + ((int64_t)(it.q_row0 + row) * a.Hq + it.head) * D;
+#pragma unroll
+        for (int c4 = 0; c4 < D / 32; ++c4) {
+          uint32_t rr[32];
+          tmem_ld32(tl + C::TM_O + c4 * 32, rr);
+          tmem_ld_wait();
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l, __uint_as_float(rr[2 * i + 1]) * inv_l);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c4 * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+          }
+        }
+        if (valid) {
+          const float m_use = (m == -INFINITY) ? 0.f : m;
+          a.lse[(int64_t)it.head * a.T + it.q_row0 + row] = (m_use + __log2f(l)) * 0.69314718055994530942f;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
+}
+
+}  // namespace
+
+template <int D>
+static cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
+                                int n_items, cudaStream_t st) {
+  using C = FwdCfg<D>;
+  static bool attr_set = false;  // per process; harmless to repeat
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  fwd_kernel<D><<<n_items, 192, C::SMEM_BYTES, st>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
+                       int n_items, cudaStream_t st) {
+  if (n_items <= 0) return cudaSuccess;
+  switch (D) {
+    case 64:
+      return launch_fwd_d<64>(tq, tk, tv, a, n_items, st);
+    case 128:
+      return launch_fwd_d<128>(tq, tk, tv, a, n_items, st);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+int fwd_key_tile(int /*D*/) { return 128; }
+int fwd_query_tile(int /*D*/) { return 128; }
+
+}  // namespace dkv

@@ -1,0 +1,80 @@
+// kernels.h -- launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "plan.h"
+
+namespace dkv {
+
+struct FwdArgs {
+  const QTileItem* items;
+  __nv_bfloat16* out;
+  float* lse;
+  int T, Hq, Hkv, window;
+  float scale_log2;  // softmax scale * log2(e)
+  uint32_t* status;
+};
+
+// Query tile rows / key tile size of the forward kernel for head dimension D.
+int fwd_query_tile(int D);
+int fwd_key_tile(int D);
+cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdArgs& a,
+                       int n_items, cudaStream_t st);
+
+struct PrepArgs {
+  const __nv_bfloat16* out;
+  const __nv_bfloat16* dout;
+  const float* lse;
+  float* delta;  // [Hq, T]
+  float* lse2;   // [Hq, T], lse * log2(e)
+  int64_t T;
+  int Hq, D;
+};
+cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st);
+
+struct DqArgs {
+  const QTileItem* items;
+  const float* delta;
+  const float* lse2;
+  __nv_bfloat16* dq;
+  int T, Hq, Hkv, window;
+  float scale_log2;  // softmax scale * log2(e)
+  float scale;       // softmax scale
+  uint32_t* status;
+};
+int dq_query_tile(int D);
+int dq_key_tile(int D);
+cudaError_t launch_dq(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                      const CUtensorMap& tdo, const DqArgs& a, int n_items, cudaStream_t st);
+
+struct DkvArgs {
+  const KVTileItem* items;
+  const QBlock* qblocks;
+  const float* delta;
+  const float* lse2;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  float* partial;  // [slot][2][key_tile][D] fp32
+  int T, Hq, Hkv, window;
+  float scale_log2;
+  float scale;
+  uint32_t* status;
+};
+int dkv_key_tile(int D);
+int dkv_query_block(int D);
+cudaError_t launch_dkv(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const DkvArgs& a, int n_items, cudaStream_t st);
+
+struct ReduceArgs {
+  const ReduceItem* items;
+  const float* partial;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int Hkv, D, key_tile;
+};
+cudaError_t launch_reduce(const ReduceArgs& a, int n_items, cudaStream_t st);
+
+}  // namespace dkv

@@ -1,0 +1,163 @@
+// plan.cpp -- host planner for the packed DualKV layout: index builder and the
+// work lists of the forward, dQ and dK/dV kernels.
+#include "plan.h"
+
+#include <algorithm>
+#include <climits>
+
+namespace dkv {
+
+const char* validate_layout(int P, int N, const int32_t* off, int Hq, int Hkv, int D) {
+  if (P < 0) return "P must be >= 0";
+  if (N < 1) return "N must be >= 1";
+  if (!off) return "R_offsets is null";
+  if (off[0] != 0) return "R_offsets[0] must be 0";
+  for (int n = 0; n < N; ++n)
+    if (off[n + 1] < off[n]) return "R_offsets must be non-decreasing";
+  if ((int64_t)P + off[N] > INT_MAX / 2) return "too many tokens";
+  if ((int64_t)P + off[N] < 1) return "no tokens";
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv) return "Hq must be a positive multiple of Hkv";
+  if (D != 64 && D != 128 && D != 512) return "D must be 64, 128 or 512";
+  return nullptr;
+}
+
+void build_index(int P, int N, const int32_t* off, int32_t* seg_id, int32_t* pos_id, int32_t* cu_rep,
+                 int32_t* rep2pack) {
+  for (int t = 0; t < P; ++t) {
+    if (seg_id) seg_id[t] = -1;
+    if (pos_id) pos_id[t] = t;
+  }
+  for (int n = 0; n < N; ++n)
+    for (int r = 0; r < off[n + 1] - off[n]; ++r) {
+      const int t = P + off[n] + r;
+      if (seg_id) seg_id[t] = n;
+      if (pos_id) pos_id[t] = P + r;
+    }
+  int64_t x = 0;
+  if (cu_rep) cu_rep[0] = 0;
+  for (int n = 0; n < N; ++n) {
+    const int len = P + off[n + 1] - off[n];
+    for (int p = 0; p < len; ++p, ++x)
+      if (rep2pack) rep2pack[x] = p < P ? p : P + off[n] + (p - P);
+    if (cu_rep) cu_rep[n + 1] = (int32_t)x;
+  }
+}
+
+namespace {
+
+struct Region {
+  int32_t row0, pos0, count;
+};
+
+std::vector<Region> regions(const Layout& L) {
+  std::vector<Region> r;
+  r.push_back({0, 0, L.P});
+  for (int n = 0; n < L.N; ++n) r.push_back({L.P + L.off[n], L.P, L.off[n + 1] - L.off[n]});
+  return r;
+}
+
+// tiles of `kr` (size `tile`) holding a key that some query in positions
+// [p_first, p_last] attends
+KeyRegion clip_keys(const Region& kr, int p_first, int p_last, int window, int tile) {
+  KeyRegion k{kr.row0, kr.pos0, kr.count, 0, 0};
+  if (kr.count <= 0) return k;
+  int64_t lo = kr.pos0;
+  if (window > 0) lo = std::max<int64_t>(lo, (int64_t)p_first - window + 1);
+  const int64_t hi = std::min<int64_t>((int64_t)kr.pos0 + kr.count - 1, p_last);
+  if (lo > hi) return k;
+  k.t_lo = (int32_t)((lo - kr.pos0) / tile);
+  k.t_hi = (int32_t)((hi - kr.pos0) / tile + 1);
+  return k;
+}
+
+}  // namespace
+
+std::vector<QTileItem> plan_qtiles(const Layout& L, int tile_rows, int key_tile) {
+  std::vector<QTileItem> items;
+  const auto regs = regions(L);
+  for (size_t qr = 0; qr < regs.size(); ++qr) {
+    const Region& q = regs[qr];
+    for (int a = 0; a < q.count; a += tile_rows) {
+      QTileItem it{};
+      it.q_row0 = q.row0 + a;
+      it.q_pos0 = q.pos0 + a;
+      it.q_rows = std::min(tile_rows, q.count - a);
+      const int p_first = it.q_pos0, p_last = it.q_pos0 + it.q_rows - 1;
+      it.reg[0] = clip_keys(regs[0], p_first, p_last, L.window, key_tile);
+      if (qr == 0)
+        it.reg[1] = KeyRegion{q.row0, q.pos0, 0, 0, 0};  // prompt queries: one region
+      else
+        it.reg[1] = clip_keys(q, p_first, p_last, L.window, key_tile);
+      for (int h = 0; h < L.Hq; ++h) {
+        it.head = h;
+        items.push_back(it);
+      }
+    }
+  }
+  std::stable_sort(items.begin(), items.end(), [](const QTileItem& a, const QTileItem& b) {
+    const int ca = (a.reg[0].t_hi - a.reg[0].t_lo) + (a.reg[1].t_hi - a.reg[1].t_lo);
+    const int cb = (b.reg[0].t_hi - b.reg[0].t_lo) + (b.reg[1].t_hi - b.reg[1].t_lo);
+    return ca > cb;
+  });
+  return items;
+}
+
+KVPlan plan_kvtiles(const Layout& L, int key_tile, int q_block, int max_iters) {
+  KVPlan plan;
+  const auto regs = regions(L);
+  const int gs = L.Hq / L.Hkv;
+  struct TileList {
+    int32_t k_row0, k_pos0, k_rows, begin, len;
+  };
+  std::vector<TileList> tiles;
+  for (size_t kr = 0; kr < regs.size(); ++kr) {
+    const Region& k = regs[kr];
+    for (int a = 0; a < k.count; a += key_tile) {
+      TileList tl{k.row0 + a, k.pos0 + a, std::min(key_tile, k.count - a), (int32_t)plan.qblocks.size(), 0};
+      const int kp_first = tl.k_pos0, kp_last = tl.k_pos0 + tl.k_rows - 1;
+      // query regions that see region kr: all of them for the prompt, else its own
+      const size_t q_lo = kr == 0 ? 0 : kr, q_hi = kr == 0 ? regs.size() : kr + 1;
+      for (size_t qr = q_lo; qr < q_hi; ++qr) {
+        const Region& q = regs[qr];
+        if (q.count <= 0) continue;
+        int64_t lo = std::max<int64_t>(kp_first, q.pos0);
+        int64_t hi = (int64_t)q.pos0 + q.count - 1;
+        if (L.window > 0) hi = std::min<int64_t>(hi, (int64_t)kp_last + L.window - 1);
+        if (lo > hi) continue;
+        const int b_lo = (int)((lo - q.pos0) / q_block), b_hi = (int)((hi - q.pos0) / q_block + 1);
+        for (int b = b_lo; b < b_hi; ++b)
+          plan.qblocks.push_back(QBlock{q.row0 + b * q_block, q.pos0 + b * q_block, std::min(q_block, q.count - b * q_block)});
+      }
+      tl.len = (int32_t)plan.qblocks.size() - tl.begin;
+      tiles.push_back(tl);
+    }
+  }
+  for (int g = 0; g < L.Hkv; ++g)
+    for (const TileList& tl : tiles) {
+      const int total = gs * tl.len;
+      const int nsplit = std::max(1, (total + max_iters - 1) / max_iters);
+      const int chunk = (total + nsplit - 1) / nsplit;
+      const int slot0 = plan.nslots;
+      int made = 0;
+      for (int lo = 0; lo < total; lo += chunk, ++made) {
+        KVTileItem it{};
+        it.k_row0 = tl.k_row0;
+        it.k_pos0 = tl.k_pos0;
+        it.k_rows = tl.k_rows;
+        it.kv_head = g;
+        it.list_begin = tl.begin;
+        it.list_len = tl.len;
+        it.it_lo = lo;
+        it.it_hi = std::min(total, lo + chunk);
+        it.partial_slot = nsplit > 1 ? plan.nslots++ : -1;
+        plan.items.push_back(it);
+      }
+      if (nsplit > 1) plan.reduces.push_back(ReduceItem{tl.k_row0, tl.k_rows, g, slot0, made, 0});
+    }
+  std::stable_sort(plan.items.begin(), plan.items.end(), [](const KVTileItem& a, const KVTileItem& b) {
+    return (a.it_hi - a.it_lo) > (b.it_hi - b.it_lo);
+  });
+  return plan;
+}
+
+}  // namespace dkv

@@ -1,0 +1,82 @@
+// plan.h -- packed-layout work lists shared by the host planner and the kernels.
+//
+// A packed micro-batch (DualKV paper, abstract: N(P+R) tokens repacked into
+// P+NR) is described by P and the segment offsets.  Queries are cut into
+// tiles that never cross a region boundary (the prompt, or one segment), and
+// each query tile attends at most two key regions: region 0 is the shared
+// prompt, region 1 the tile's own segment.  Key tiles are cut the same way.
+#pragma once
+#include <stdint.h>
+
+#include <vector>
+
+namespace dkv {
+
+// One contiguous run of keys: rows [row0, row0+count) of the packed layout,
+// with positions pos0 .. pos0+count-1.  Tiles are taken from row0 in steps of
+// the kernel's key-tile size; tiles [t_lo, t_hi) hold at least one key that the
+// owning query tile attends.
+struct KeyRegion {
+  int32_t row0, pos0, count, t_lo, t_hi;
+};
+
+// Forward / dQ work item: one query tile of one q-head.
+struct QTileItem {
+  int32_t q_row0;  // first packed row
+  int32_t q_pos0;  // its position
+  int32_t q_rows;  // valid rows (<= tile rows); rows past it belong to another region
+  int32_t head;    // q-head
+  KeyRegion reg[2];
+};
+
+// A block of query rows inside one region, used by the dK/dV walk.
+struct QBlock {
+  int32_t q_row0, q_pos0, q_rows;
+};
+
+// dK/dV work item: one key tile of one kv-head, walking iterations
+// [it_lo, it_hi) of the tile's query list.  Iteration `it` is group head
+// it / list_len and query block qblocks[list_begin + it % list_len].
+struct KVTileItem {
+  int32_t k_row0, k_pos0, k_rows, kv_head;
+  int32_t list_begin, list_len;
+  int32_t it_lo, it_hi;
+  int32_t partial_slot;  // -1: write bf16 dk/dv directly; else fp32 partial slot
+  int32_t pad_;
+};
+
+// Fixed-order reduction of split prompt key tiles.
+struct ReduceItem {
+  int32_t k_row0, k_rows, kv_head, slot0, nslots, pad_;
+};
+
+struct Layout {
+  int P, N;
+  std::vector<int32_t> off;  // N+1
+  int Hq, Hkv, D, window;
+  int64_t T() const { return (int64_t)P + off[N]; }
+};
+
+// Returns an error string, or nullptr when the layout is valid.
+const char* validate_layout(int P, int N, const int32_t* off, int Hq, int Hkv, int D);
+
+// Query tiles of `tile_rows` rows and their key regions for key tiles of
+// `key_tile` keys, heaviest first (by key tiles visited), ties by (head, row).
+std::vector<QTileItem> plan_qtiles(const Layout& L, int tile_rows, int key_tile);
+
+struct KVPlan {
+  std::vector<KVTileItem> items;     // heaviest first
+  std::vector<QBlock> qblocks;       // concatenated per-key-tile query lists
+  std::vector<ReduceItem> reduces;   // one per split key tile
+  int nslots = 0;                    // fp32 partial slots (each key_tile x D for dK and for dV)
+};
+
+// Key tiles of `key_tile` keys, query blocks of `q_block` rows.  A key tile
+// whose walk exceeds `max_iters` iterations is split into contiguous chunks.
+KVPlan plan_kvtiles(const Layout& L, int key_tile, int q_block, int max_iters);
+
+// Host index builder (see dualkv_build_index).
+void build_index(int P, int N, const int32_t* off, int32_t* seg_id, int32_t* pos_id, int32_t* cu_rep,
+                 int32_t* rep2pack);
+
+}  // namespace dkv

@@ -1,0 +1,210 @@
+"""ctypes binding of libdualkv.so (declared in include/dualkv.h).
+
+Argument marshalling only: every step of the attention path runs in the
+library's CUDA kernels.  The functions keep the C names and signatures
+(tensors in place of raw pointers); ``forward``/``backward`` add buffer
+allocation on top.  If the library is missing, loading raises: there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdualkv.so")
+
+DUALKV_OK = 0
+DUALKV_ERR_INVALID = 1
+DUALKV_ERR_ALIGN = 2
+DUALKV_ERR_WORKSPACE = 3
+DUALKV_ERR_CUDA = 4
+DUALKV_ERR_DEVICE = 5
+DUALKV_ERR_UNSUPPORTED = 6
+
+# every symbol the header declares
+EXPORTS = ("dualkv_fwd", "dualkv_bwd_workspace_bytes", "dualkv_bwd", "dualkv_build_index", "dualkv_rho",
+           "dualkv_pairs", "dualkv_check_status", "dualkv_error_string", "dualkv_release")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class DualKVError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {error_string(code)} (code {code})")
+
+
+def load(path: Optional[str] = None):
+    """Load libdualkv.so; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build it with shared_prompt_exact_gb300.build.build()")
+        lib = ctypes.CDLL(p)
+        vp, ci, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        lib.dualkv_fwd.argtypes = [vp, vp, vp, ci, ci, i32p, ci, ci, ci, cf, ci, vp, vp, vp]
+        lib.dualkv_fwd.restype = ci
+        lib.dualkv_bwd_workspace_bytes.argtypes = [ci, ci, i32p, ci, ci, ci, ci]
+        lib.dualkv_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.dualkv_bwd.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, i32p, ci, ci, ci, cf, ci, vp, vp, vp, vp,
+                                   ctypes.c_size_t, vp]
+        lib.dualkv_bwd.restype = ci
+        lib.dualkv_build_index.argtypes = [ci, ci, i32p, i32p, i32p, i32p, i32p]
+        lib.dualkv_build_index.restype = ci
+        lib.dualkv_rho.argtypes = [ci, ci, i32p]
+        lib.dualkv_rho.restype = ctypes.c_double
+        lib.dualkv_pairs.argtypes = [ci, ci, i32p, ci]
+        lib.dualkv_pairs.restype = ctypes.c_int64
+        lib.dualkv_check_status.argtypes = [vp]
+        lib.dualkv_check_status.restype = ci
+        lib.dualkv_error_string.argtypes = [ci]
+        lib.dualkv_error_string.restype = ctypes.c_char_p
+        lib.dualkv_release.argtypes = []
+        lib.dualkv_release.restype = None
+        _lib = lib
+        return lib
+
+
+def error_string(code: int) -> str:
+    return load().dualkv_error_string(int(code)).decode()
+
+
+def _offsets(R_offsets: Sequence[int]):
+    arr = (ctypes.c_int32 * len(R_offsets))(*[int(x) for x in R_offsets])
+    return arr
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check_dev(name, t, dtype):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _raise(code, where):
+    if code != DUALKV_OK:
+        raise DualKVError(code, where)
+
+
+def dualkv_fwd(q, k, v, P, N, R_offsets, Hq, Hkv, D, scale, window, out, lse, stream=None) -> None:
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
+                        ("out", out, torch.bfloat16), ("lse", lse, torch.float32)):
+        _check_dev(name, t, dt)
+    off = _offsets(R_offsets)
+    rc = load().dualkv_fwd(_ptr(q), _ptr(k), _ptr(v), int(P), int(N), off, int(Hq), int(Hkv), int(D),
+                           float(scale), int(window), _ptr(out), _ptr(lse), _stream(stream))
+    _raise(rc, "dualkv_fwd")
+
+
+def dualkv_bwd_workspace_bytes(P, N, R_offsets, Hq, Hkv, D, window) -> int:
+    return int(load().dualkv_bwd_workspace_bytes(int(P), int(N), _offsets(R_offsets), int(Hq), int(Hkv), int(D),
+                                                  int(window)))
+
+
+def dualkv_bwd(q, k, v, out, lse, dout, P, N, R_offsets, Hq, Hkv, D, scale, window, dq, dk, dv, workspace,
+               workspace_bytes=None, stream=None) -> None:
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
+                        ("out", out, torch.bfloat16), ("lse", lse, torch.float32), ("dout", dout, torch.bfloat16),
+                        ("dq", dq, torch.bfloat16), ("dk", dk, torch.bfloat16), ("dv", dv, torch.bfloat16)):
+        _check_dev(name, t, dt)
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = load().dualkv_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), int(P), int(N),
+                           _offsets(R_offsets), int(Hq), int(Hkv), int(D), float(scale), int(window), _ptr(dq),
+                           _ptr(dk), _ptr(dv), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    _raise(rc, "dualkv_bwd")
+
+
+def dualkv_build_index(P, N, R_offsets):
+    """Host index builder: returns (seg_id, pos_id, cu_seqlens_rep, rep2pack) as int32 CPU tensors."""
+    T = int(P) + int(R_offsets[N])
+    n_rep = int(N) * int(P) + int(R_offsets[N])
+    seg = torch.empty(T, dtype=torch.int32)
+    pos = torch.empty(T, dtype=torch.int32)
+    cu = torch.empty(int(N) + 1, dtype=torch.int32)
+    r2p = torch.empty(max(n_rep, 1), dtype=torch.int32)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    rc = load().dualkv_build_index(int(P), int(N), _offsets(R_offsets),
+                                   ctypes.cast(seg.data_ptr(), i32p), ctypes.cast(pos.data_ptr(), i32p),
+                                   ctypes.cast(cu.data_ptr(), i32p), ctypes.cast(r2p.data_ptr(), i32p))
+    _raise(rc, "dualkv_build_index")
+    return seg, pos, cu, r2p[:n_rep]
+
+
+def dualkv_rho(P, N, R_offsets) -> float:
+    return float(load().dualkv_rho(int(P), int(N), _offsets(R_offsets)))
+
+
+def dualkv_pairs(P, N, R_offsets, window=0) -> int:
+    return int(load().dualkv_pairs(int(P), int(N), _offsets(R_offsets), int(window)))
+
+
+def dualkv_check_status(stream=None) -> None:
+    _raise(load().dualkv_check_status(_stream(stream)), "dualkv_check_status")
+
+
+def dualkv_release() -> None:
+    load().dualkv_release()
+
+
+# ------------------------------------------------------------------ convenience
+def forward(q, k, v, P, R_offsets, window=0, scale=None, stream=None):
+    """Allocate out/lse and run dualkv_fwd. q [T,Hq,D], k/v [T,Hkv,D] bf16 CUDA."""
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    N = len(R_offsets) - 1
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    out = torch.empty_like(q)
+    lse = torch.empty(Hq, T, dtype=torch.float32, device=q.device)
+    dualkv_fwd(q, k, v, P, N, R_offsets, Hq, Hkv, D, scale, window, out, lse, stream)
+    return out, lse
+
+
+def workspace_for(P, R_offsets, Hq, Hkv, D, window=0, device="cuda"):
+    nbytes = dualkv_bwd_workspace_bytes(P, len(R_offsets) - 1, R_offsets, Hq, Hkv, D, window)
+    if nbytes == 0:
+        raise DualKVError(DUALKV_ERR_INVALID, "dualkv_bwd_workspace_bytes")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def backward(q, k, v, out, lse, dout, P, R_offsets, window=0, scale=None, workspace=None, stream=None):
+    """Allocate dq/dk/dv (and workspace if not given) and run dualkv_bwd."""
+    T, Hq, D = q.shape
+    Hkv = k.shape[1]
+    N = len(R_offsets) - 1
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    if workspace is None:
+        workspace = workspace_for(P, R_offsets, Hq, Hkv, D, window, q.device)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    dualkv_bwd(q, k, v, out, lse, dout, P, N, R_offsets, Hq, Hkv, D, scale, window, dq, dk, dv, workspace,
+               None, stream)
+    return dq, dk, dv

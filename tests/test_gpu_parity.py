@@ -1,0 +1,234 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances (GPU output widened to fp64, compared over the compared slice):
+  O     max-abs <= 1e-2 and normwise relative <= 5e-3
+  LSE   max-abs <= 1e-3
+  dQ/dK/dV  normwise relative <= 2e-2 each
+Small and medium layouts are compared on every row and head.  The full-size
+workloads are compared on sampled rows / keys of two GQA groups (the oracle
+computes each sampled output by the definition), on conservation properties
+that hold at any size, and against the same kernels run on the replicated
+layout (P = 0, one sequence per response) folded on the host.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from shared_prompt_exact_gb300 import build as pbuild
+from shared_prompt_exact_gb300 import dualkv
+from shared_prompt_exact_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+O_ABS, O_REL, LSE_ABS, G_REL = 1e-2, 5e-3, 1e-3, 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    pbuild.build()
+    dualkv.load()
+
+
+def relF(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def run_gpu(w, q, k, v, do, backward=True):
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    out, lse = dualkv.forward(qd, kd, vd, w.P, w.offsets, w.window, w.scale)
+    res = dict(out=out, lse=lse)
+    if backward:
+        dod = do.cuda()
+        dq, dk, dv = dualkv.backward(qd, kd, vd, out, lse, dod, w.P, w.offsets, w.window, w.scale)
+        res.update(dq=dq, dk=dk, dv=dv)
+    dualkv.dualkv_check_status()
+    return res
+
+
+def check_full(w, g, ref):
+    out = g["out"].double().cpu().numpy()
+    lse = g["lse"].double().cpu().numpy()
+    assert np.max(np.abs(out - ref["out"])) <= O_ABS
+    assert relF(out, ref["out"]) <= O_REL
+    assert np.max(np.abs(lse - ref["lse"])) <= LSE_ABS
+    for key in ("dq", "dk", "dv"):
+        got = g[key].double().cpu().numpy()
+        assert relF(got, ref[key]) <= G_REL, (key, relF(got, ref[key]))
+
+
+SMALL = [
+    # name, P, R, Hq, Hkv, D, window
+    ("tiny-config", 64, [32] * 4, 2, 2, 64, 0),
+    ("ragged-gqa", 300, [200, 0, 129, 1, 64], 4, 2, 128, 0),
+    ("aligned", 128, [128, 128], 2, 2, 128, 0),
+    ("no-prompt", 0, [257, 3], 2, 1, 64, 0),
+    ("one-seg-p1", 1, [130], 2, 2, 128, 0),
+    ("window-boundary", 129, [127, 129], 4, 1, 128, 64),
+    ("window-1", 200, [70, 300], 2, 2, 64, 1),
+    ("empty-segments", 127, [0, 5, 0], 2, 2, 128, 0),
+    ("gqa4-window", 400, [33] * 6, 8, 2, 128, 150),
+    ("split-prompt-tiles", 128, [512] * 16, 4, 1, 64, 0),
+    ("long-prompt-d128", 1000, [100, 300, 7], 2, 1, 128, 0),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_parity_small(case):
+    name, P, R, Hq, Hkv, D, W = case
+    w = wl.WORKLOADS["tiny"] if name == "tiny-config" else wl.custom(P, R, Hq, Hkv, D, W, seed=hash(name) % 100000)
+    q, k, v, do = wl.draw_inputs(w)
+    g = run_gpu(w, q, k, v, do)
+    ref = oracle.dualkv(w.P, w.N, w.offsets, w.Hq, w.Hkv, w.D, w.scale, w.window, q, k, v, do)
+    assert ref["prompt_invariant"] == 1
+    check_full(w, g, ref)
+
+
+def test_determinism_bitwise():
+    w = wl.custom(128, [512] * 16, 4, 1, 64, 0, seed=7)  # includes split prompt key tiles
+    q, k, v, do = wl.draw_inputs(w)
+    a = run_gpu(w, q, k, v, do)
+    b = run_gpu(w, q, k, v, do)
+    for key in ("out", "lse", "dq", "dk", "dv"):
+        assert torch.equal(a[key], b[key]), key
+
+
+def test_outputs_fully_overwritten():
+    w = wl.custom(70, [40, 90], 2, 2, 128, 0, seed=3)
+    q, k, v, do = wl.draw_inputs(w)
+    qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    outs = []
+    for fill in (0.0, float("nan")):
+        out = torch.full_like(qd, fill)
+        lse = torch.full((w.Hq, w.T), fill, device="cuda")
+        dualkv.dualkv_fwd(qd, kd, vd, w.P, w.N, w.offsets, w.Hq, w.Hkv, w.D, w.scale, 0, out, lse)
+        dq, dk, dv = (torch.full_like(x, fill) for x in (qd, kd, vd))
+        ws = dualkv.workspace_for(w.P, w.offsets, w.Hq, w.Hkv, w.D)
+        ws.fill_(255)
+        dualkv.dualkv_bwd(qd, kd, vd, out, lse, dod, w.P, w.N, w.offsets, w.Hq, w.Hkv, w.D, w.scale, 0, dq, dk, dv, ws)
+        dualkv.dualkv_check_status()
+        outs.append((out, lse, dq, dk, dv))
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------ full size
+FULL_D128 = ["qwen16", "grpo32", "dapo32"]
+
+
+def sample_rows(w, rng, n_random=8):
+    off = w.offsets
+    rows = {0, 1, w.P // 2, w.P - 1} if w.P > 0 else set()
+    for n in (0, w.N // 2, w.N - 1):
+        a, b = w.P + off[n], w.P + off[n + 1]
+        if b > a:
+            rows |= {a, (a + b) // 2, b - 1}
+    rows |= set(int(x) for x in rng.integers(0, w.T, n_random))
+    return sorted(r for r in rows if 0 <= r < w.T)
+
+
+def sample_response_keys(w, rng, n_random=6):
+    off = w.offsets
+    keys = set()
+    for n in (0, w.N // 2, w.N - 1):
+        a, b = w.P + off[n], w.P + off[n + 1]
+        if b > a:
+            keys |= {a, b - 1, (a + b) // 2}
+    keys |= set(int(x) for x in rng.integers(w.P, w.T, n_random))
+    return sorted(keys)
+
+
+def groups_to_check(w, rng):
+    return sorted({int(rng.integers(0, w.Hkv)), w.Hkv - 1})
+
+
+def check_sampled(w, q, k, v, do, g, prompt_keys=False):
+    rng = np.random.default_rng(w.seed)
+    out = g["out"].cpu()
+    lse = g["lse"].cpu()
+    dq = g["dq"].cpu()
+    dk = g["dk"].cpu()
+    dv = g["dv"].cpu()
+    gs = w.Hq // w.Hkv
+    rows = sample_rows(w, rng)
+    for grp in groups_to_check(w, rng):
+        for h in range(grp * gs, grp * gs + gs):
+            o_r, l_r, dq_r = oracle.query_rows(w.P, w.N, w.offsets, w.Hq, w.Hkv, w.D, w.scale, w.window, h, rows,
+                                               q, k, v, do)
+            o_g = out[rows, h].double().numpy()
+            assert np.max(np.abs(o_g - o_r)) <= O_ABS
+            assert relF(o_g, o_r) <= O_REL
+            assert np.max(np.abs(lse[h, rows].double().numpy() - l_r)) <= LSE_ABS
+            assert relF(dq[rows, h].double().numpy(), dq_r) <= G_REL
+        keys = sample_response_keys(w, rng)
+        if prompt_keys and w.P > 0:
+            keys = sorted(set(keys) | {w.P - 1, w.P - 2, w.P - 64, w.P - 129})
+        dk_r, dv_r = oracle.key_rows(w.P, w.N, w.offsets, w.Hq, w.Hkv, w.D, w.scale, w.window, grp, keys,
+                                     q, k, v, do)
+        assert relF(dk[keys, grp].double().numpy(), dk_r) <= G_REL
+        assert relF(dv[keys, grp].double().numpy(), dv_r) <= G_REL
+
+
+def check_conservation(w, do, g):
+    # sum_j dV_j = sum over the group's heads and all packed rows of dO_i  (rows of P sum to 1)
+    # sum_j dK_j = 0                                                          (rows of dS sum to 0)
+    gs = w.Hq // w.Hkv
+    dv = g["dv"].double()
+    dk = g["dk"].double()
+    dod = do.cuda().double()
+    for grp in range(w.Hkv):
+        want = dod[:, grp * gs:(grp + 1) * gs].sum(dim=(0, 1))
+        got = dv[:, grp].sum(dim=0)
+        assert float((got - want).norm() / want.norm()) <= G_REL
+        s = dk[:, grp].sum(dim=0)
+        assert float(s.norm()) <= 1e-2 * float(dk[:, grp].norm()) * math.sqrt(w.D)
+
+
+def fold_replicated(w, x_rep):
+    """Sum replicated prompt rows over replicas; response rows map 1:1 (x_rep on GPU)."""
+    off = w.offsets
+    out = torch.zeros((w.T,) + tuple(x_rep.shape[1:]), dtype=torch.float32, device=x_rep.device)
+    pos = 0
+    for n in range(w.N):
+        Rn = off[n + 1] - off[n]
+        out[: w.P] += x_rep[pos: pos + w.P].float()
+        out[w.P + off[n]: w.P + off[n + 1]] = x_rep[pos + w.P: pos + w.P + Rn].float()
+        pos += w.P + Rn
+    return out
+
+
+def check_packed_vs_replicated(w, q, k, v, do, g):
+    wr = w.replicated()
+    qr, kr, vr = (wl.replicate_rows(w, x.cuda()) for x in (q, k, v))
+    dor = wl.replicate_rows(w, do.cuda()).clone()
+    pos = 0
+    off = w.offsets
+    for n in range(w.N):  # prompt upstream gradient carried by replica 0 only
+        if n > 0:
+            dor[pos: pos + w.P] = 0
+        pos += w.P + off[n + 1] - off[n]
+    out_r, lse_r = dualkv.forward(qr, kr, vr, wr.P, wr.offsets, wr.window, wr.scale)
+    dq_r, dk_r, dv_r = dualkv.backward(qr, kr, vr, out_r, lse_r, dor, wr.P, wr.offsets, wr.window, wr.scale)
+    dualkv.dualkv_check_status()
+    # forward: every replica's rows equal the packed rows
+    out_p = wl.replicate_rows(w, g["out"]).float()
+    assert float((out_r.float() - out_p).norm() / out_p.norm()) <= O_REL
+    assert float((out_r.float() - out_p).abs().max()) <= O_ABS
+    for name, rep in (("dq", dq_r), ("dk", dk_r), ("dv", dv_r)):
+        folded = fold_replicated(w, rep)
+        got = g[name].float()
+        assert float((got - folded).norm() / folded.norm()) <= G_REL, name
+
+
+@pytest.mark.parametrize("name", FULL_D128)
+def test_parity_full_size_sampled(name):
+    w = wl.WORKLOADS[name]
+    q, k, v, do = wl.draw_inputs(w)
+    g = run_gpu(w, q, k, v, do)
+    check_sampled(w, q, k, v, do, g, prompt_keys=(name == "grpo32"))
+    check_conservation(w, do, g)
+    check_packed_vs_replicated(w, q, k, v, do, g)
