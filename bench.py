@@ -1,0 +1,467 @@
+#!/usr/bin/env python
+"""DualKV shared-prompt attention benchmark on GB300.
+
+One step = one DualKV forward + backward (dualkv_fwd + dualkv_bwd) over one
+packed micro-batch of the chosen workload (default: the Qwen3-8B GRPO-shaped
+layer, P=6144, N=32, R=2048, Hq=32, Hkv=8, D=128, causal), inputs resident in
+HBM.  The metric is useful TFLOP/s: forward 4*D*Hq*pairs + backward
+10*D*Hq*pairs per step, where pairs counts attended (query, key) pairs of one
+head with every packed query row counted once.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl dualkv|reference]
+
+With N > 1 (launched by torch.distributed.run) every rank runs an independent
+replica of the step on its own GPU (no collective on the data path), timing is
+the max over ranks and the value is the total over ranks ("weak" scaling).
+``--impl reference`` times the fp64 CPU oracle (the only reference this method
+has) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from shared_prompt_exact_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "DualKV attn fwd+bwd useful TFLOP/s & % BF16 tensor peak, N=32 P=6144 R=2048"
+UNIT = "TFLOP/s"
+
+# algorithmic tensor-core FLOPs per attended pair per head (x D) of each kernel
+KERNEL_FLOPS_PER_PAIR = {"fwd": 4, "dkv": 8, "dq": 6}
+
+
+# ------------------------------------------------------------------ helpers
+def useful_flops(pairs, D, Hq):
+    return 4.0 * D * Hq * pairs, 10.0 * D * Hq * pairs
+
+
+def layout_pairs(w):
+    from shared_prompt_exact_gb300 import dualkv
+    return dualkv.dualkv_pairs(w.P, w.N, w.offsets, w.window)
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return dict(bf16_burst=float(m["bf16_tflops"]), bf16_sustained=float(m["bf16_tflops_sustained"]),
+                    hbm_gbs=float(m["hbm_gbs"]), source="measured")
+    except Exception:
+        return dict(bf16_burst=1900.0, bf16_sustained=1700.0, hbm_gbs=6800.0, source="fallback")
+
+
+def source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "shared_prompt_exact_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current sources."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}_ncu.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"source_digest:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != source_digest():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the GPU is under load."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.marks = []
+
+    def start(self):
+        sel = self._selector()
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200"] + sel, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _selector(self):
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+            if uuid:
+                return ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            pass
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            return ["-i", vis.split(",")[self.dev]]
+        return ["-i", str(self.dev)]
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+
+    def summary(self, t0, t1):
+        def parse(rows):
+            sm, mx, reasons = [], [], set()
+            names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+            for _, line in rows:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(nm)
+            return sm, mx, reasons
+        window = [r for r in self.lines if t0 <= r[0] <= t1]
+        sm, mx, reasons = parse(window)
+        scope = "timed region"
+        if len(sm) < 3:
+            sm, mx, reasons = parse([r for r in self.lines if r[0] >= t0])
+            scope = "timed region and the measurement phases after it"
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "scope": "unavailable"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "scope": scope}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x, world, device):
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(ms_local, flops_per_rank, world, device):
+    """Whole-job throughput of `world` independent replicas: every rank does
+    flops_per_rank per step; the job's step time is the slowest rank's."""
+    ms = max_over_ranks(ms_local, world, device)
+    return ms, world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ oracle (CPU baseline / reference arm)
+def oracle_sample(w, q, k, v, do, n_seg=2):
+    """A bounded sample of the workload: the prompt, the first n_seg responses and
+    the first GQA group (Hq/Hkv q-heads, one kv-head)."""
+    gs = w.Hq // w.Hkv
+    n_seg = min(n_seg, w.N)
+    off = w.offsets[: n_seg + 1]
+    T = w.P + off[-1]
+    return dict(P=w.P, N=n_seg, off=off, Hq=gs, Hkv=1, D=w.D, scale=w.scale, window=w.window,
+                q=q[:T, :gs].contiguous(), k=k[:T, :1].contiguous(), v=v[:T, :1].contiguous(),
+                do=do[:T, :gs].contiguous())
+
+
+def time_oracle(s):
+    import oracle
+    from oracle import index as oindex
+    pairs = oindex.pairs(s["P"], s["off"], s["window"])
+    flops = 14.0 * s["D"] * s["Hq"] * pairs
+    t0 = time.perf_counter()
+    oracle.dualkv(s["P"], s["N"], s["off"], s["Hq"], s["Hkv"], s["D"], s["scale"], s["window"], s["q"], s["k"],
+                  s["v"], s["do"])
+    dt = time.perf_counter() - t0
+    return flops, dt, oracle.num_threads()
+
+
+def sample_text(w, s):
+    return (f"{w.name}: prompt P={s['P']} with the first {s['N']} of {w.N} responses "
+            f"(R_offsets {s['off']}), first GQA group ({s['Hq']} q-heads, 1 kv-head), D={s['D']}, "
+            f"fwd+bwd; useful FLOPs counted on the sample's packed pairs")
+
+
+def run_reference(args, w):
+    world, rank, local = dist_setup()
+    if rank != 0:
+        return 0
+    q, k, v, do = wl.draw_inputs(w)
+    s = oracle_sample(w, q, k, v, do, n_seg=args.oracle_segments)
+    for _ in range(args.warmup):
+        time_oracle(s)
+    times = []
+    flops = 0.0
+    cores = 1
+    for _ in range(args.steps):
+        flops, dt, cores = time_oracle(s)
+        times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    value = flops / (ms * 1e-3) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "P": w.P, "N": w.N, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "window": w.window, "sample": sample_text(w, s)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample_text(w, s)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_dualkv(args, w):
+    from shared_prompt_exact_gb300 import build as pbuild
+    from shared_prompt_exact_gb300 import dualkv
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pbuild.build()
+    dualkv.load()
+
+    q_h, k_h, v_h, do_h = wl.draw_inputs(w)
+    q, k, v, do = (x.to(dev) for x in (q_h, k_h, v_h, do_h))
+    T, Hq, Hkv, D = w.T, w.Hq, w.Hkv, w.D
+    out = torch.empty_like(q)
+    lse = torch.empty(Hq, T, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = dualkv.workspace_for(w.P, w.offsets, Hq, Hkv, D, w.window, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        dualkv.dualkv_fwd(q, k, v, w.P, w.N, w.offsets, Hq, Hkv, D, w.scale, w.window, out, lse, stream)
+
+    def bwd():
+        dualkv.dualkv_bwd(q, k, v, out, lse, do, w.P, w.N, w.offsets, Hq, Hkv, D, w.scale, w.window, dq, dk, dv, ws,
+                          None, stream)
+
+    def step():
+        fwd()
+        bwd()
+
+    pairs = layout_pairs(w)
+    f_fwd, f_bwd = useful_flops(pairs, D, Hq)
+    f_step = f_fwd + f_bwd
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    dualkv.dualkv_check_status(stream)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+
+    def timed(fn, reps):
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        return e0.elapsed_time(e1) / reps
+
+    t_start = time.time()
+    ms_step = timed(step, args.steps)
+    t_end = time.time()
+    ms_step, value = aggregate(ms_step, f_step, world, dev)
+    ms_fwd = max_over_ranks(timed(fwd, args.steps), world, dev)
+    ms_bwd = max_over_ranks(timed(bwd, args.steps), world, dev)
+    dualkv.dualkv_check_status(stream)
+
+    # per-kernel durations (events on the launching stream, recorded by the library)
+    prof_steps = max(1, min(args.steps, 5))
+    dualkv.dualkv_profile_read()
+    dualkv.dualkv_profile_enable(True)
+    for _ in range(prof_steps):
+        step()
+    torch.cuda.synchronize(dev)
+    kt = dualkv.dualkv_profile_read()
+    dualkv.dualkv_profile_enable(False)
+    launches_per_step = sum(n for _, n in kt.values()) / prof_steps
+    dom = max(kt, key=lambda kk: kt[kk][0])
+    pk = peaks()
+    roofline = None
+    if dom in KERNEL_FLOPS_PER_PAIR:
+        per_launch_flops = KERNEL_FLOPS_PER_PAIR[dom] * D * Hq * pairs
+        avg_ms = kt[dom][0] / kt[dom][1]
+        achieved = per_launch_flops / (avg_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": pk["bf16_sustained"],
+                    "unit": "TFLOP/s", "frac": achieved / pk["bf16_sustained"],
+                    "traffic": ncu_traffic(dom, w.name),
+                    "peak_source": pk["source"] + " bf16 sustained (kernel timed inside a multi-step loop)",
+                    "avg_launch_ms": avg_ms, "algorithmic_flops_per_launch": per_launch_flops}
+    kernels = {kk: {"ms_per_launch": (ms / n if n else None), "launches": n} for kk, (ms, n) in kt.items()}
+
+    # end to end through the C ABI with host buffers: pinned H2D of the step's
+    # inputs, forward + backward, D2H of every output
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda x: x.pin_memory()  # noqa: E731
+        hq, hk, hv, hdo = (pin(x) for x in (q_h, k_h, v_h, do_h))
+        ho, hl, hdq, hdk, hdv = (torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (out, lse, dq, dk, dv))
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
+        d2h = sum(x.numel() * x.element_size() for x in (ho, hl, hdq, hdk, hdv))
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            do.copy_(hdo, non_blocking=True)
+            step()
+            for hdst, src in ((ho, out), (hl, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
+                hdst.copy_(src, non_blocking=True)
+
+        e2e_step()
+        ms_e2e = max_over_ranks(timed(e2e_step, max(1, min(args.steps, 5))), world, dev)
+        e2e = {"value": world * f_step / (ms_e2e * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
+
+    # the same kernels on the replicated layout (prompt copied into every sequence)
+    replicated = None
+    if not args.no_replicated:
+        wr = w.replicated()
+        del out, dq
+        torch.cuda.empty_cache()
+        qr, kr, vr, dor = (wl.replicate_rows(w, x) for x in (q, k, v, do))
+        outr = torch.empty_like(qr)
+        lser = torch.empty(Hq, wr.T, dtype=torch.float32, device=dev)
+        dqr, dkr, dvr = torch.empty_like(qr), torch.empty_like(kr), torch.empty_like(vr)
+        wsr = dualkv.workspace_for(wr.P, wr.offsets, Hq, Hkv, D, wr.window, dev)
+
+        def rstep():
+            dualkv.dualkv_fwd(qr, kr, vr, wr.P, wr.N, wr.offsets, Hq, Hkv, D, wr.scale, wr.window, outr, lser, stream)
+            dualkv.dualkv_bwd(qr, kr, vr, outr, lser, dor, wr.P, wr.N, wr.offsets, Hq, Hkv, D, wr.scale, wr.window,
+                              dqr, dkr, dvr, wsr, None, stream)
+
+        rstep()
+        ms_rep = max_over_ranks(timed(rstep, max(1, min(args.steps, 5))), world, dev)
+        dualkv.dualkv_check_status(stream)
+        pairs_r = layout_pairs(wr)
+        fr = sum(useful_flops(pairs_r, D, Hq))
+        replicated = {"ms_per_step": ms_rep, "tflops_own_pairs": fr / (ms_rep * 1e-3) / 1e12,
+                      "tflops_effective": f_step / (ms_rep * 1e-3) / 1e12, "pairs_per_head": pairs_r,
+                      "speedup_packed_over_replicated": ms_rep / ms_step}
+        del qr, kr, vr, dor, outr, dqr, dkr, dvr, wsr
+
+    sampler.stop()
+    clocks = sampler.summary(t_start, t_end)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        s = oracle_sample(w, q_h, k_h, v_h, do_h, n_seg=args.oracle_segments)
+        flops_s, dt, cores = time_oracle(s)
+        cpu = {"value": flops_s / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": sample_text(w, s), "seconds": dt}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "P": w.P, "N": w.N, "R": (w.R[0] if len(set(w.R)) == 1 else "ragged"),
+                       "Hq": Hq, "Hkv": Hkv, "D": D, "window": w.window, "packed_tokens": T,
+                       "replicated_tokens": w.T_replicated, "pairs_per_head": pairs,
+                       "l2": "no flush: inputs larger than L2 (q+k+v+dO = %.2f GB)" % (
+                           sum(x.numel() * x.element_size() for x in (q, k, v, do)) / 1e9),
+                       "parallelism": f"replicas x{world}"},
+            "pct_bf16_peak": {"measured_burst": value / world / pk["bf16_burst"],
+                              "measured_sustained": value / world / pk["bf16_sustained"],
+                              "nominal_2250": value / world / 2250.0},
+            "fwd": {"ms": ms_fwd, "tflops": f_fwd / (ms_fwd * 1e-3) / 1e12},
+            "bwd": {"ms": ms_bwd, "tflops": f_bwd / (ms_bwd * 1e-3) / 1e12},
+            "rho": dualkv.dualkv_rho(w.P, w.N, w.offsets),
+            "kernels": kernels,
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "replicated": replicated,
+            "gpu_launches": int(round(launches_per_step * args.steps)),
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("dualkv", "reference"), default="dualkv")
+    ap.add_argument("--config", default="grpo32", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--oracle-segments", type=int, default=2)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-replicated", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    w = wl.WORKLOADS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_dualkv(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

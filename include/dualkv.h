@@ -134,7 +134,38 @@ int dualkv_check_status(void* stream);
 /* Static, NUL-terminated description of a return code. */
 const char* dualkv_error_string(int code);
 
-/* Frees the plan cache and status words.  Not safe while launches are pending. */
+/*
+ * Per-kernel timing for benchmarks.  While enabled (on != 0), every kernel the
+ * library launches is bracketed by CUDA events recorded on the caller's
+ * stream.  dualkv_profile_read() waits for the recorded events, adds each
+ * kernel's elapsed milliseconds and launch count into ms[kind] and
+ * launches[kind] for kind = DUALKV_KERNEL_* (arrays of DUALKV_KERNEL_KINDS
+ * entries, host memory), and forgets the records.  Returns DUALKV_OK or
+ * DUALKV_ERR_CUDA.
+ */
+#define DUALKV_KERNEL_FWD 0
+#define DUALKV_KERNEL_PREP 1
+#define DUALKV_KERNEL_DKV 2
+#define DUALKV_KERNEL_REDUCE 3
+#define DUALKV_KERNEL_DQ 4
+#define DUALKV_KERNEL_KINDS 5
+int dualkv_profile_enable(int on);
+int dualkv_profile_read(double* ms, int64_t* launches);
+
+/*
+ * Self-test of the kernels' failure path (no counterpart in the paper; it
+ * exists so that timeout handling can be tested without faulting a GPU).
+ * Launches one CTA of 64 threads that wait, with the same bounded mbarrier
+ * wait every kernel uses but a limit of limit_ns nanoseconds (1 ms .. 10 s),
+ * on a barrier that nothing completes.  The wait gives up, records a timeout
+ * in the status word and the kernel returns; dualkv_check_status() then
+ * reports DUALKV_ERR_DEVICE and the context stays usable.  Returns
+ * DUALKV_ERR_INVALID for a limit out of range, DUALKV_ERR_CUDA if the launch
+ * fails, else DUALKV_OK.
+ */
+int dualkv_selftest_timeout(uint64_t limit_ns, void* stream);
+
+/* Frees the plan cache, status words and timing events.  Not safe while launches are pending. */
 void dualkv_release(void);
 
 #ifdef __cplusplus

@@ -147,6 +147,39 @@ int get_plan(int P, int N, const int32_t* off, int Hq, int Hkv, int D, int windo
   return DUALKV_OK;
 }
 
+// ---------------------------------------------------------------- kernel timing
+struct TimedLaunch {
+  int kind;
+  cudaEvent_t start, stop;
+};
+bool g_profile = false;
+std::vector<TimedLaunch> g_timed;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Runs `launch` on stream `st`, bracketed by events when timing is enabled.
+template <typename F>
+cudaError_t timed(int kind, cudaStream_t st, F&& launch) {
+  if (!g_profile) return launch();
+  TimedLaunch t{kind, take_event(), take_event()};
+  if (!t.start || !t.stop) return cudaErrorMemoryAllocation;
+  cudaEventRecord(t.start, st);
+  cudaError_t e = launch();
+  cudaEventRecord(t.stop, st);
+  g_timed.push_back(t);
+  return e;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
@@ -188,7 +221,9 @@ int dualkv_fwd(const void* q, const void* k, const void* v, int P, int N, const 
     return DUALKV_ERR_CUDA;
   FwdArgs a{pl->fwd_items, static_cast<__nv_bfloat16*>(out), lse, (int)T, Hq, Hkv, window <= 0 ? 0 : window,
             scale * 1.4426950408889634f, status};
-  if (launch_fwd(D, tq, tk, tv, a, pl->n_fwd, static_cast<cudaStream_t>(stream)) != cudaSuccess) return DUALKV_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (timed(DUALKV_KERNEL_FWD, st, [&] { return launch_fwd(D, tq, tk, tv, a, pl->n_fwd, st); }) != cudaSuccess)
+    return DUALKV_ERR_CUDA;
   return DUALKV_OK;
 }
 
@@ -229,7 +264,7 @@ int dualkv_bwd(const void* q, const void* k, const void* v, const void* out, con
   const float sl2 = scale * 1.4426950408889634f;
 
   PrepArgs pa{static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, delta, lse2, T, Hq, D};
-  if (launch_prep(pa, st) != cudaSuccess) return DUALKV_ERR_CUDA;
+  if (timed(DUALKV_KERNEL_PREP, st, [&] { return launch_prep(pa, st); }) != cudaSuccess) return DUALKV_ERR_CUDA;
 
   CUtensorMap tq, tk, tv, tdo;
   if (make_tmap(&tq, q, T, Hq, D, dkv_query_block(D)) || make_tmap(&tk, k, T, Hkv, D, dkv_key_tile(D)) ||
@@ -237,11 +272,13 @@ int dualkv_bwd(const void* q, const void* k, const void* v, const void* out, con
     return DUALKV_ERR_CUDA;
   DkvArgs ka{pl->kv_items, pl->qblocks, delta, lse2, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
              partial, (int)T, Hq, Hkv, W, sl2, scale, status};
-  if (launch_dkv(D, tq, tk, tv, tdo, ka, pl->n_kv, st) != cudaSuccess) return DUALKV_ERR_CUDA;
+  if (timed(DUALKV_KERNEL_DKV, st, [&] { return launch_dkv(D, tq, tk, tv, tdo, ka, pl->n_kv, st); }) != cudaSuccess)
+    return DUALKV_ERR_CUDA;
   if (pl->n_reduce > 0) {
     ReduceArgs ra{pl->reduces, partial, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), Hkv, D,
                   dkv_key_tile(D)};
-    if (launch_reduce(ra, pl->n_reduce, st) != cudaSuccess) return DUALKV_ERR_CUDA;
+    if (timed(DUALKV_KERNEL_REDUCE, st, [&] { return launch_reduce(ra, pl->n_reduce, st); }) != cudaSuccess)
+      return DUALKV_ERR_CUDA;
   }
 
   CUtensorMap tq2, tk2, tv2, tdo2;
@@ -249,7 +286,8 @@ int dualkv_bwd(const void* q, const void* k, const void* v, const void* out, con
       make_tmap(&tv2, v, T, Hkv, D, dq_key_tile(D)) || make_tmap(&tdo2, dout, T, Hq, D, dq_query_tile(D)))
     return DUALKV_ERR_CUDA;
   DqArgs qa{pl->dq_items, delta, lse2, static_cast<__nv_bfloat16*>(dq), (int)T, Hq, Hkv, W, sl2, scale, status};
-  if (launch_dq(D, tq2, tk2, tv2, tdo2, qa, pl->n_dq, st) != cudaSuccess) return DUALKV_ERR_CUDA;
+  if (timed(DUALKV_KERNEL_DQ, st, [&] { return launch_dq(D, tq2, tk2, tv2, tdo2, qa, pl->n_dq, st); }) != cudaSuccess)
+    return DUALKV_ERR_CUDA;
   return DUALKV_OK;
 }
 
@@ -329,8 +367,52 @@ const char* dualkv_error_string(int code) {
   }
 }
 
+int dualkv_selftest_timeout(uint64_t limit_ns, void* stream) {
+  if (limit_ns < 1000000ull || limit_ns > 10000000000ull) return DUALKV_ERR_INVALID;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DUALKV_ERR_CUDA;
+  uint32_t* status = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (status_word(dev, &status)) return DUALKV_ERR_CUDA;
+  }
+  if (launch_selftest_timeout(limit_ns, status, static_cast<cudaStream_t>(stream)) != cudaSuccess) return DUALKV_ERR_CUDA;
+  return DUALKV_OK;
+}
+
+int dualkv_profile_enable(int on) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_profile = on != 0;
+  return DUALKV_OK;
+}
+
+int dualkv_profile_read(double* ms, int64_t* launches) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  int rc = DUALKV_OK;
+  for (const TimedLaunch& t : g_timed) {
+    float e = 0.f;
+    if (cudaEventSynchronize(t.stop) != cudaSuccess || cudaEventElapsedTime(&e, t.start, t.stop) != cudaSuccess) {
+      rc = DUALKV_ERR_CUDA;
+    } else if (t.kind >= 0 && t.kind < DUALKV_KERNEL_KINDS) {
+      if (ms) ms[t.kind] += e;
+      if (launches) launches[t.kind] += 1;
+    }
+    g_event_pool.push_back(t.start);
+    g_event_pool.push_back(t.stop);
+  }
+  g_timed.clear();
+  return rc;
+}
+
 void dualkv_release(void) {
   std::lock_guard<std::mutex> lock(g_mu);
+  for (const TimedLaunch& t : g_timed) {
+    g_event_pool.push_back(t.start);
+    g_event_pool.push_back(t.stop);
+  }
+  g_timed.clear();
+  for (cudaEvent_t e : g_event_pool) cudaEventDestroy(e);
+  g_event_pool.clear();
   g_plans.clear();
   for (auto& kv : g_status) cudaFree(kv.second);
   g_status.clear();

@@ -607,7 +607,28 @@ __global__ void __launch_bounds__(256) reduce_kernel(const ReduceArgs a) {
   }
 }
 
+// ---------------------------------------------------------------- failure-path self-test
+__global__ void __launch_bounds__(64) selftest_timeout_kernel(uint64_t limit_ns, uint32_t* status) {
+  __shared__ uint64_t never;  // expects two arrivals; only thread 0 ever arrives
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&never, 2);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_arrive(&never);
+  FailState fs{&abort_flag, status};
+  mbar_wait(&never, 0, fs, limit_ns);
+  __syncthreads();
+}
+
 }  // namespace
+
+cudaError_t launch_selftest_timeout(uint64_t limit_ns, uint32_t* status, cudaStream_t st) {
+  selftest_timeout_kernel<<<1, 64, 0, st>>>(limit_ns, status);
+  return cudaGetLastError();
+}
 
 int dq_query_tile(int /*D*/) { return 128; }
 int dq_key_tile(int /*D*/) { return 64; }

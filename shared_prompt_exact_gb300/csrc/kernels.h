@@ -77,4 +77,7 @@ struct ReduceArgs {
 };
 cudaError_t launch_reduce(const ReduceArgs& a, int n_items, cudaStream_t st);
 
+// One CTA waits on an mbarrier that nothing completes, with a bounded wait of limit_ns.
+cudaError_t launch_selftest_timeout(uint64_t limit_ns, uint32_t* status, cudaStream_t st);
+
 }  // namespace dkv

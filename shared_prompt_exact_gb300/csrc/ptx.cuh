@@ -76,14 +76,15 @@ __device__ __forceinline__ void raise_failure(const FailState& fs, uint32_t code
 
 // Bounded wait for phase `parity` of `bar`.  Returns false on timeout or when
 // another role of the CTA already aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const FailState& fs) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const FailState& fs,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 63u) {
       if (*fs.abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         raise_failure(fs, kDevErrTimeout);
         return false;
       }

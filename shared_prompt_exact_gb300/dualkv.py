@@ -29,7 +29,9 @@ DUALKV_ERR_UNSUPPORTED = 6
 
 # every symbol the header declares
 EXPORTS = ("dualkv_fwd", "dualkv_bwd_workspace_bytes", "dualkv_bwd", "dualkv_build_index", "dualkv_rho",
-           "dualkv_pairs", "dualkv_check_status", "dualkv_error_string", "dualkv_release")
+           "dualkv_pairs", "dualkv_check_status", "dualkv_error_string", "dualkv_profile_enable",
+           "dualkv_profile_read", "dualkv_selftest_timeout", "dualkv_release")
+KERNEL_KINDS = ("fwd", "prep", "dkv", "reduce", "dq")
 
 _lock = threading.Lock()
 _lib = None
@@ -70,6 +72,12 @@ def load(path: Optional[str] = None):
         lib.dualkv_check_status.restype = ci
         lib.dualkv_error_string.argtypes = [ci]
         lib.dualkv_error_string.restype = ctypes.c_char_p
+        lib.dualkv_profile_enable.argtypes = [ci]
+        lib.dualkv_profile_enable.restype = ci
+        lib.dualkv_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)]
+        lib.dualkv_profile_read.restype = ci
+        lib.dualkv_selftest_timeout.argtypes = [ctypes.c_uint64, vp]
+        lib.dualkv_selftest_timeout.restype = ci
         lib.dualkv_release.argtypes = []
         lib.dualkv_release.restype = None
         _lib = lib
@@ -168,6 +176,23 @@ def dualkv_pairs(P, N, R_offsets, window=0) -> int:
 
 def dualkv_check_status(stream=None) -> None:
     _raise(load().dualkv_check_status(_stream(stream)), "dualkv_check_status")
+
+
+def dualkv_profile_enable(on: bool) -> None:
+    _raise(load().dualkv_profile_enable(1 if on else 0), "dualkv_profile_enable")
+
+
+def dualkv_profile_read():
+    """{kernel kind: (total ms, launches)} of the launches timed since the last read."""
+    n = len(KERNEL_KINDS)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    _raise(load().dualkv_profile_read(ms, cnt), "dualkv_profile_read")
+    return {KERNEL_KINDS[i]: (float(ms[i]), int(cnt[i])) for i in range(n)}
+
+
+def dualkv_selftest_timeout(limit_ns: int, stream=None) -> None:
+    _raise(load().dualkv_selftest_timeout(int(limit_ns), _stream(stream)), "dualkv_selftest_timeout")
 
 
 def dualkv_release() -> None:

@@ -105,3 +105,8 @@ def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(4, 2, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         dualkv.dualkv_fwd(x, x, x, 2, 1, [0, 2], 2, 2, 64, 0.125, 0, x, torch.zeros(2, 4), None)
+
+
+def test_selftest_rejects_out_of_range_limit(lib):
+    assert lib.dualkv_selftest_timeout(10, None) == dualkv.DUALKV_ERR_INVALID
+    assert lib.dualkv_selftest_timeout(100 * 10**9, None) == dualkv.DUALKV_ERR_INVALID
