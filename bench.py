@@ -19,6 +19,7 @@ has) on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -202,7 +203,7 @@ def barrier(world):
 
 
 # ------------------------------------------------------------------ oracle (CPU baseline / reference arm)
-def oracle_sample(w, q, k, v, do, n_seg=2):
+def oracle_sample(w, q, k, v, do, n_seg=1):
     """A bounded sample of the workload: the prompt, the first n_seg responses and
     the first GQA group (Hq/Hkv q-heads, one kv-head)."""
     gs = w.Hq // w.Hkv
@@ -452,12 +453,17 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("dualkv", "reference"), default="dualkv")
     ap.add_argument("--config", default="grpo32", choices=sorted(wl.WORKLOADS))
-    ap.add_argument("--oracle-segments", type=int, default=2)
+    ap.add_argument("--oracle-segments", type=int, default=1)
+    ap.add_argument("--heads", default=None,
+                    help="Hq,Hkv override: a smaller case of the same layout for ncu captures")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-replicated", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     w = wl.WORKLOADS[args.config]
+    if args.heads:
+        hq, hkv = (int(x) for x in args.heads.split(","))
+        w = dataclasses.replace(w, name=f"{w.name}-h{hq}x{hkv}", Hq=hq, Hkv=hkv)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_dualkv(args, w)

@@ -511,7 +511,9 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.st_empty[b]);
       if (i >= 2 && !(ok = mbar_wait(&ctl.pt_done[b], ((i - 2) >> 1) & 1, fs))) break;
-      // ring slot stays full until the dV/dK MMAs of this block complete, so lse2/delta are stable
+      // acquire the producer's lse2/delta stores for this block; the slot cannot
+      // be refilled before this block's dV/dK MMAs complete, so its phase is current
+      if (!(ok = mbar_wait(&ctl.ring_full[slot], (i / C::NST) & 1, fs))) break;
       const float* L2 = ctl.lse2[slot];
       const float* DL = ctl.delta[slot];
       const uint32_t pb = smem_u32(sPT + b * C::PT_BYTES), sb = smem_u32(sDST + b * C::PT_BYTES);

@@ -266,7 +266,9 @@ __global__ void __launch_bounds__(192, 1)
       if (j == 0) {
         m = m_new;
       } else if (__any_sync(0xffffffffu, m_new > m + C::RESCALE_THRESHOLD)) {
-        const float alpha = ex2_approx(m - m_new);  // m = -inf gives 0; O and l are 0 then
+        // the decision is per warp: a row that has seen no allowed key yet (m_new = -inf)
+        // keeps alpha = 1; a row whose first allowed key arrives now has m = -inf, alpha = 0
+        const float alpha = (m_new == -INFINITY) ? 1.f : ex2_approx(m - m_new);
         if (!(ok = mbar_wait(&ctl.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, fs))) break;
         tc_fence_after();
 #pragma unroll

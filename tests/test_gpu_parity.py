@@ -1,7 +1,9 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
 
 Tolerances (GPU output widened to fp64, compared over the compared slice):
-  O     max-abs <= 1e-2 and normwise relative <= 5e-3
+  O     max-abs <= 1e-2 beyond the output's own bf16 rounding (half an ulp of the
+        exact value; above |O| = 4 that half ulp alone exceeds 1e-2), and
+        normwise relative <= 5e-3
   LSE   max-abs <= 1e-3
   dQ/dK/dV  normwise relative <= 2e-2 each
 Small and medium layouts are compared on every row and head.  The full-size
@@ -11,6 +13,7 @@ that hold at any size, and against the same kernels run on the replicated
 layout (P = 0, one sequence per response) folded on the host.
 """
 import math
+import zlib
 
 import numpy as np
 import pytest
@@ -30,6 +33,20 @@ O_ABS, O_REL, LSE_ABS, G_REL = 1e-2, 5e-3, 1e-3, 2e-2
 def _lib():
     pbuild.build()
     dualkv.load()
+
+
+def bf16_half_ulp(x):
+    """Half the bf16 spacing at |x| (8 significant bits)."""
+    ax = np.maximum(np.abs(np.asarray(x, dtype=np.float64)), 2.0 ** -126)
+    return np.ldexp(1.0, (np.floor(np.log2(ax)) - 8).astype(np.int64))
+
+
+def assert_o_close(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    excess = np.abs(got - ref) - bf16_half_ulp(ref)
+    assert np.max(excess) <= O_ABS, float(np.max(excess))
+    assert relF(got, ref) <= O_REL, relF(got, ref)
 
 
 def relF(a, b):
@@ -53,8 +70,7 @@ def run_gpu(w, q, k, v, do, backward=True):
 def check_full(w, g, ref):
     out = g["out"].double().cpu().numpy()
     lse = g["lse"].double().cpu().numpy()
-    assert np.max(np.abs(out - ref["out"])) <= O_ABS
-    assert relF(out, ref["out"]) <= O_REL
+    assert_o_close(out, ref["out"])
     assert np.max(np.abs(lse - ref["lse"])) <= LSE_ABS
     for key in ("dq", "dk", "dv"):
         got = g[key].double().cpu().numpy()
@@ -69,7 +85,6 @@ SMALL = [
     ("no-prompt", 0, [257, 3], 2, 1, 64, 0),
     ("one-seg-p1", 1, [130], 2, 2, 128, 0),
     ("window-boundary", 129, [127, 129], 4, 1, 128, 64),
-    ("window-1", 200, [70, 300], 2, 2, 64, 1),
     ("empty-segments", 127, [0, 5, 0], 2, 2, 128, 0),
     ("gqa4-window", 400, [33] * 6, 8, 2, 128, 150),
     ("split-prompt-tiles", 128, [512] * 16, 4, 1, 64, 0),
@@ -80,12 +95,31 @@ SMALL = [
 @pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
 def test_parity_small(case):
     name, P, R, Hq, Hkv, D, W = case
-    w = wl.WORKLOADS["tiny"] if name == "tiny-config" else wl.custom(P, R, Hq, Hkv, D, W, seed=hash(name) % 100000)
+    w = wl.WORKLOADS["tiny"] if name == "tiny-config" else wl.custom(P, R, Hq, Hkv, D, W, seed=zlib.crc32(name.encode()) % 100000)
     q, k, v, do = wl.draw_inputs(w)
     g = run_gpu(w, q, k, v, do)
     ref = oracle.dualkv(w.P, w.N, w.offsets, w.Hq, w.Hkv, w.D, w.scale, w.window, q, k, v, do)
     assert ref["prompt_invariant"] == 1
     check_full(w, g, ref)
+
+
+def test_window_one_attends_only_itself():
+    # W = 1: P_ii = 1, so O = v exactly, LSE = scale q.k, dV = sum of the group's dO,
+    # and dS = 0 makes dQ and dK vanish (only rounding of Delta remains)
+    w = wl.custom(200, [70, 300], 4, 2, 64, 1, seed=11)
+    q, k, v, do = wl.draw_inputs(w)
+    g = run_gpu(w, q, k, v, do)
+    gs = w.Hq // w.Hkv
+    out = g["out"].cpu()
+    for h in range(w.Hq):
+        assert torch.equal(out[:, h], v[:, h // gs])
+    lse_ref = (q.double() * k.double().repeat_interleave(gs, dim=1)).sum(-1).T * w.scale
+    assert float((g["lse"].cpu().double() - lse_ref).abs().max()) <= LSE_ABS
+    dv_ref = do.double().reshape(w.T, w.Hkv, gs, w.D).sum(2)
+    assert relF(g["dv"].double().cpu().numpy(), dv_ref.numpy()) <= G_REL
+    scale_ref = float(dv_ref.norm())
+    assert float(g["dq"].double().norm()) <= G_REL * scale_ref
+    assert float(g["dk"].double().norm()) <= G_REL * scale_ref
 
 
 def test_determinism_bitwise():
@@ -120,15 +154,18 @@ def test_outputs_fully_overwritten():
 FULL_D128 = ["qwen16", "grpo32", "dapo32"]
 
 
-def sample_rows(w, rng, n_random=8):
+def sample_rows(w, rng, n_random=24):
+    """(uniform random rows, boundary rows).  The uniform sample estimates the
+    normwise error of the whole tensor; boundary rows (first prompt rows, segment
+    starts / middles / ends) are edge cases checked on the tensor's scale."""
     off = w.offsets
-    rows = {0, 1, w.P // 2, w.P - 1} if w.P > 0 else set()
+    edge = {0, 1, w.P // 2, w.P - 1} if w.P > 0 else set()
     for n in (0, w.N // 2, w.N - 1):
         a, b = w.P + off[n], w.P + off[n + 1]
         if b > a:
-            rows |= {a, (a + b) // 2, b - 1}
-    rows |= set(int(x) for x in rng.integers(0, w.T, n_random))
-    return sorted(r for r in rows if 0 <= r < w.T)
+            edge |= {a, (a + b) // 2, b - 1}
+    uni = sorted(set(int(x) for x in rng.integers(0, w.T, n_random)))
+    return uni, sorted(r for r in edge if 0 <= r < w.T)
 
 
 def sample_response_keys(w, rng, n_random=6):
@@ -154,16 +191,20 @@ def check_sampled(w, q, k, v, do, g, prompt_keys=False):
     dk = g["dk"].cpu()
     dv = g["dv"].cpu()
     gs = w.Hq // w.Hkv
-    rows = sample_rows(w, rng)
+    uni, edge = sample_rows(w, rng)
+    rows = uni + edge
+    nu = len(uni)
     for grp in groups_to_check(w, rng):
         for h in range(grp * gs, grp * gs + gs):
             o_r, l_r, dq_r = oracle.query_rows(w.P, w.N, w.offsets, w.Hq, w.Hkv, w.D, w.scale, w.window, h, rows,
                                                q, k, v, do)
-            o_g = out[rows, h].double().numpy()
-            assert np.max(np.abs(o_g - o_r)) <= O_ABS
-            assert relF(o_g, o_r) <= O_REL
+            assert_o_close(out[rows, h].double().numpy(), o_r)
             assert np.max(np.abs(lse[h, rows].double().numpy() - l_r)) <= LSE_ABS
-            assert relF(dq[rows, h].double().numpy(), dq_r) <= G_REL
+            dq_g = dq[rows, h].double().numpy()
+            assert relF(dq_g[:nu], dq_r[:nu]) <= G_REL
+            rms_row = np.linalg.norm(dq_r[:nu]) / math.sqrt(nu)
+            for i in range(nu, len(rows)):
+                assert np.linalg.norm(dq_g[i] - dq_r[i]) <= G_REL * max(rms_row, np.linalg.norm(dq_r[i])), rows[i]
         keys = sample_response_keys(w, rng)
         if prompt_keys and w.P > 0:
             keys = sorted(set(keys) | {w.P - 1, w.P - 2, w.P - 64, w.P - 129})
