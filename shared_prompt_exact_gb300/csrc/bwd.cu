@@ -63,28 +63,46 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepArgs a) {
   }
 }
 
+// Shared structure of the dQ and dK/dV kernels (320 threads):
+//   warp 0      TMA producer
+//   warp 1      TMEM owner and MMA issuer (one thread; descriptors are computed
+//               once per tile and advanced by constant adds inside unrolled loops)
+//   warps 2-9   compute: warps w and w+4 share TMEM lane quarter w % 4 (one row
+//               per thread) and split the 64 columns of a block into halves
+// The first GEMM pair writes two double-buffered fp32 blocks to TMEM; the
+// compute warps read them, and write the bf16 result (dS, or P^T and dS^T)
+// back over the same buffer, where the second GEMM reads it as its A operand.
+// Half h reads fp32 columns [32h, 32h+32) and writes its 32 bf16 values
+// (16 packed columns) to [32h, 32h+16): a warp only overwrites columns it has
+// read itself, so the two halves need no synchronisation with each other.
+// K-step k of the second GEMM (16 values) therefore sits at column
+// 32 (k / 2) + 8 (k % 2).  tcgen05.mma ops issued by one thread execute in
+// issue order, so a buffer is rewritten by the next first-pair GEMM only
+// after the second GEMM that reads it.
+constexpr int kBwdThreads = 320;
+
+__device__ __forceinline__ uint32_t packed_kstep_col(int k) { return 32u * (k >> 1) + 8u * (k & 1); }
+
 // ---------------------------------------------------------------- dQ
 template <int D>
 struct DqCfg {
   static constexpr int BM = 128, BN = 64;
   static constexpr int KCH = D / 64;
-  static constexpr int Q_BYTES = BM * D * 2;         // Q and dO tiles
+  static constexpr int Q_BYTES = BM * D * 2;         // Q and dO tiles (resident)
   static constexpr int TILE_BYTES = BN * D * 2;      // one K or V tile
-  static constexpr int DS_BYTES = BM * BN * 2;
-  static constexpr int NST = (D == 128) ? 8 : 12;
+  static constexpr int NST = (D == 128) ? 10 : 16;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = OFF_Q + Q_BYTES;
-  static constexpr int OFF_DS = OFF_DO + Q_BYTES;
-  static constexpr int OFF_RING = OFF_DS + 2 * DS_BYTES;
+  static constexpr int OFF_RING = OFF_DO + Q_BYTES;
   static constexpr int SMEM_BYTES = OFF_RING + NST * TILE_BYTES + 1024;
   static constexpr uint32_t TM_S = 0, TM_DP = 2 * BN, TM_DQ = 4 * BN, TM_COLS = 512;
 };
 
 struct DqSmemCtl {
   uint64_t q_full;
-  uint64_t ring_full[12], ring_empty[12];
-  uint64_t s_full[2], s_empty[2], ds_full[2], ds_done[2];
-  uint64_t drain;
+  uint64_t ring_full[16], ring_empty[16];
+  uint64_t s_full[2], ds_full[2];
+  uint64_t acc_done, drain;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -101,7 +119,7 @@ __device__ __forceinline__ void qtile_of(const QTileItem& it, int j, int& r, int
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const DqArgs a) {
   using C = DqCfg<D>;
@@ -110,7 +128,6 @@ __global__ void __launch_bounds__(192, 1)
   __shared__ DqSmemCtl ctl;
   uint8_t* sQ = smem + C::OFF_Q;
   uint8_t* sDO = smem + C::OFF_DO;
-  uint8_t* sDS = smem + C::OFF_DS;
   uint8_t* sRing = smem + C::OFF_RING;
 
   const QTileItem it = a.items[blockIdx.x];
@@ -128,10 +145,9 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl.s_full[i], 1);
-      mbar_init(&ctl.s_empty[i], 4);
-      mbar_init(&ctl.ds_full[i], 4);
-      mbar_init(&ctl.ds_done[i], 1);
+      mbar_init(&ctl.ds_full[i], 8);
     }
+    mbar_init(&ctl.acc_done, 1);
     mbar_init(&ctl.drain, 1);
     fence_mbar_init();
   }
@@ -145,7 +161,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = ctl.tmem_base;
 
   if (warp == 0) {
-    // producer: Q and dO once, then K_j, V_j for every key tile
+    // producer: Q and dO once, then K_j, V_j (ring index 2j, 2j+1)
     if (lane == 0 && nt > 0) {
       mbar_arrive_expect_tx(&ctl.q_full, 2 * C::Q_BYTES);
       for (int c = 0; c < C::KCH; ++c) {
@@ -160,8 +176,7 @@ __global__ void __launch_bounds__(192, 1)
         const int key_row = it.reg[r].row0 + t * C::BN;
         for (int kind = 0; kind < 2; ++kind, ++idx) {
           const int slot = idx % C::NST;
-          const uint32_t ph = (idx / C::NST) & 1;
-          if (!(ok = mbar_wait(&ctl.ring_empty[slot], ph ^ 1, fs))) break;
+          if (!(ok = mbar_wait(&ctl.ring_empty[slot], ((idx / C::NST) & 1) ^ 1, fs))) break;
           mbar_arrive_expect_tx(&ctl.ring_full[slot], C::TILE_BYTES);
           uint8_t* dst = sRing + slot * C::TILE_BYTES;
           const CUtensorMap* tm = kind == 0 ? &tmK : &tmV;
@@ -177,59 +192,70 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else if (warp == 1) {
-    // MMA issuer: S_j = Q K_j^T, dP_j = dO V_j^T, then dQ += dS_{j-1} K_{j-1}
-    if (lane == 0 && nt > 0) {
+    // MMA issuer: S_j = Q K_j^T, dP_j = dO V_j^T (SS, N = 64), then dQ += dS_{j-1} K_{j-1} (TS, N = D).
+    // The whole warp runs the loop so descriptors stay warp-uniform; one elected
+    // lane issues each batch of MMAs and its commits.
+    if (nt > 0) {
       constexpr uint32_t idS = idesc_bf16(128, C::BN, 0, 0);
       constexpr uint32_t idQ = idesc_bf16(128, D, 0, 1);
-      const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO), aDS = smem_u32(sDS), aRing = smem_u32(sRing);
+      const uint64_t dQd = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dDOd = sdesc_sw128(smem_u32(sDO), 16, 1024);
+      const uint32_t aRing = smem_u32(sRing);
       bool ok = mbar_wait(&ctl.q_full, 0, fs);
       tc_fence_after();
       for (int j = 0; j <= nt && ok; ++j) {
         if (j < nt) {
-          const int b = j & 1;
+          const uint32_t b = j & 1;
           const int ik = 2 * j, iv = 2 * j + 1;
-          if (!(ok = mbar_wait(&ctl.s_empty[b], ((j >> 1) & 1) ^ 1, fs))) break;
           if (!(ok = mbar_wait(&ctl.ring_full[ik % C::NST], (ik / C::NST) & 1, fs))) break;
           if (!(ok = mbar_wait(&ctl.ring_full[iv % C::NST], (iv / C::NST) & 1, fs))) break;
           tc_fence_after();
-          const uint32_t kb = aRing + (ik % C::NST) * C::TILE_BYTES, vb = aRing + (iv % C::NST) * C::TILE_BYTES;
+          const uint64_t kd = sdesc_sw128(aRing + (ik % C::NST) * C::TILE_BYTES, 16, 1024);
+          const uint64_t vd = sdesc_sw128(aRing + (iv % C::NST) * C::TILE_BYTES, 16, 1024);
+          const uint32_t tS = tmem + C::TM_S + b * C::BN, tP = tmem + C::TM_DP + b * C::BN;
+          if (elect_one()) {
 #pragma unroll
-          for (int c = 0; c < C::KCH; ++c)
+            for (int c = 0; c < C::KCH; ++c)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              mma_bf16_ss(tmem + C::TM_S + b * C::BN, sdesc_sw128(aQ + c * C::BM * 128 + k * 32, 16, 1024),
-                          sdesc_sw128(kb + c * C::BN * 128 + k * 32, 16, 1024), idS, (c | k) != 0);
-            }
-#pragma unroll
-          for (int c = 0; c < C::KCH; ++c)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              mma_bf16_ss(tmem + C::TM_DP + b * C::BN, sdesc_sw128(aDO + c * C::BM * 128 + k * 32, 16, 1024),
-                          sdesc_sw128(vb + c * C::BN * 128 + k * 32, 16, 1024), idS, (c | k) != 0);
-            }
-          mma_commit(&ctl.ring_empty[iv % C::NST]);
-          mma_commit(&ctl.s_full[b]);
+              for (int k = 0; k < 4; ++k) {
+                mma_bf16_ss(tS, sdesc_add(dQd, c * C::BM * 128 + k * 32), sdesc_add(kd, c * C::BN * 128 + k * 32),
+                            idS, (c | k) != 0);
+                mma_bf16_ss(tP, sdesc_add(dDOd, c * C::BM * 128 + k * 32), sdesc_add(vd, c * C::BN * 128 + k * 32),
+                            idS, (c | k) != 0);
+              }
+            mma_commit(&ctl.ring_empty[iv % C::NST]);
+            mma_commit(&ctl.s_full[b]);
+          }
+          __syncwarp();
         }
         if (j >= 1) {
-          const int jj = j - 1, b = jj & 1, ik = 2 * jj;
+          const int jj = j - 1, ik = 2 * jj;
+          const uint32_t b = jj & 1;
           if (!(ok = mbar_wait(&ctl.ds_full[b], (jj >> 1) & 1, fs))) break;
           tc_fence_after();
-          const uint32_t kb = aRing + (ik % C::NST) * C::TILE_BYTES;
-          const uint32_t db = aDS + b * C::DS_BYTES;
+          const uint64_t kmn = sdesc_sw128(aRing + (ik % C::NST) * C::TILE_BYTES, C::BN * 128, 1024);
+          const uint32_t tA = tmem + C::TM_S + b * C::BN;
+          const uint32_t acc0 = jj > 0 ? 1u : 0u;
+          if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < C::BN / 16; ++k)
-            mma_bf16_ss(tmem + C::TM_DQ, sdesc_sw128(db + k * 32, 16, 1024),
-                        sdesc_sw128(kb + k * 16 * 128, C::BN * 128, 1024), idQ, (jj > 0 || k > 0) ? 1u : 0u);
-          mma_commit(&ctl.ring_empty[ik % C::NST]);
-          mma_commit(&ctl.ds_done[b]);
+            for (int k = 0; k < C::BN / 16; ++k)
+              mma_bf16_ts(tmem + C::TM_DQ, tA + packed_kstep_col(k), sdesc_add(kmn, k * 16 * 128), idQ,
+                          k > 0 ? 1u : acc0);
+            mma_commit(&ctl.ring_empty[ik % C::NST]);
+          }
+          __syncwarp();
         }
       }
-      mma_commit(&ctl.drain);
+      if (elect_one()) {
+        if (ok) mma_commit(&ctl.acc_done);
+        mma_commit(&ctl.drain);
+      }
+      __syncwarp();
       mbar_wait_drain(&ctl.drain, 0, kWaitLimitNs);
     }
   } else {
-    // dS warps: thread <-> query row
-    const uint32_t wq = warp & 3;
+    // compute warps: thread <-> query row, half <-> 32 key columns of each 64-key block
+    const uint32_t wq = warp & 3, half = (warp - 2) >> 2;
     const int row = (int)(wq * 32 + lane);
     const uint32_t tl = tmem + ((wq * 32) << 16);
     const int qpos = it.q_pos0 + row;
@@ -240,67 +266,59 @@ __global__ void __launch_bounds__(192, 1)
     const float sl2 = a.scale_log2;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
-      const int b = j & 1;
-      if (!(ok = mbar_wait(&ctl.s_full[b], (j >> 1) & 1, fs))) break;
-      tc_fence_after();
+      const uint32_t b = j & 1;
       int r, t;
       qtile_of(it, j, r, t);
       const KeyRegion& kr = it.reg[r];
-      const int kl0 = t * C::BN;
+      const int kl0 = t * C::BN + 32 * (int)half;
       int lo = 0;
       if (a.window > 0) lo = max(0, qpos - a.window + 1 - kr.pos0);
       const int hi = min(kr.count - 1, qpos - kr.pos0);
-      const int clo = lo - kl0, chi = hi - kl0;
-      uint32_t sr[64], dr[64];
-      tmem_ld32(tl + C::TM_S + b * C::BN, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(tl + C::TM_S + b * C::BN + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_ld32(tl + C::TM_DP + b * C::BN, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
-      tmem_ld32(tl + C::TM_DP + b * C::BN + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+      const int clo = lo - kl0, chi = hi - kl0;  // allowed columns of this half
+      const bool full = (clo <= 0) && (chi >= 31);
+      if (!(ok = mbar_wait(&ctl.s_full[b], (j >> 1) & 1, fs))) break;
+      tc_fence_after();
+      uint32_t sr[32], dr[32];
+      tmem_ld32(tl + C::TM_S + b * C::BN + 32 * half, sr);
+      tmem_ld32(tl + C::TM_DP + b * C::BN + 32 * half, dr);
       tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.s_empty[b]);
-      if (j >= 2 && !(ok = mbar_wait(&ctl.ds_done[b], ((j - 2) >> 1) & 1, fs))) break;
-      const uint32_t db = smem_u32(sDS + b * C::DS_BYTES);
+      uint32_t w[16];
 #pragma unroll
-      for (int pc = 0; pc < 8; ++pc) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = pc * 8 + e * 2;
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, -lse2));
+      for (int e = 0; e < 16; ++e) {
+        const int c = 2 * e;
+        float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2));
+        float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, -lse2));
+        if (!full) {
           p0 = (c < clo || c > chi) ? 0.f : p0;
           p1 = (c + 1 < clo || c + 1 > chi) ? 0.f : p1;
-          const float d0 = p0 * (__uint_as_float(dr[c]) - delta);
-          const float d1 = p1 * (__uint_as_float(dr[c + 1]) - delta);
-          w[e] = pack_bf16x2(d0, d1);
         }
-        st_shared_v4(db + sw128_offset(row, pc), w[0], w[1], w[2], w[3]);
+        w[e] = pack_bf16x2(p0 * (__uint_as_float(dr[c]) - delta), p1 * (__uint_as_float(dr[c + 1]) - delta));
       }
-      fence_proxy_async_smem();
+      tmem_st16(tl + C::TM_S + b * C::BN + 32 * half, w);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.ds_full[b]);
     }
     if (ok && nt > 0) {
-      ok = mbar_wait(&ctl.ds_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, fs);
+      ok = mbar_wait(&ctl.acc_done, 0, fs);
       tc_fence_after();
       if (ok) {
         __nv_bfloat16* qrow = a.dq + ((int64_t)(it.q_row0 + row) * a.Hq + it.head) * D;
 #pragma unroll
-        for (int c4 = 0; c4 < D / 32; ++c4) {
+        for (int c4 = 0; c4 < D / 64; ++c4) {
+          const int col = (int)half * (D / 2) + c4 * 32;
           uint32_t rr[32];
-          tmem_ld32(tl + C::TM_DQ + c4 * 32, rr);
+          tmem_ld32(tl + C::TM_DQ + col, rr);
           tmem_ld_wait();
-          uint32_t w[16];
+          uint32_t o[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i)
-            w[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * a.scale, __uint_as_float(rr[2 * i + 1]) * a.scale);
+            o[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * a.scale, __uint_as_float(rr[2 * i + 1]) * a.scale);
           if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(qrow + c4 * 32);
+            uint4* dst = reinterpret_cast<uint4*>(qrow + col);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
           }
         }
       }
@@ -316,35 +334,33 @@ __global__ void __launch_bounds__(192, 1)
 template <int D>
 struct DkvCfg {
   static constexpr int BN = 128;  // keys per tile (MMA M)
-  static constexpr int BQ = 64;   // queries per block (MMA N of S^T, K of dV/dK)
+  static constexpr int BQ = 64;   // queries per block (N of the first pair, K of the second)
   static constexpr int KCH = D / 64;
   static constexpr int KV_BYTES = BN * D * 2;
-  static constexpr int QB_BYTES = BQ * D * 2;            // one Q or dO block
-  static constexpr int UNIT_BYTES = 2 * QB_BYTES;        // Q block + dO block
-  static constexpr int PT_BYTES = BN * BQ * 2;           // P^T or dS^T (bf16)
-  static constexpr int NST = (D == 128) ? 2 : 4;
+  static constexpr int QB_BYTES = BQ * D * 2;      // one Q or dO block
+  static constexpr int UNIT_BYTES = 2 * QB_BYTES;  // Q block + dO block
+  static constexpr int NST = (D == 128) ? 4 : 8;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_BYTES;
-  static constexpr int OFF_PT = OFF_V + KV_BYTES;        // 2 buffers
-  static constexpr int OFF_DST = OFF_PT + 2 * PT_BYTES;  // 2 buffers
-  static constexpr int OFF_RING = OFF_DST + 2 * PT_BYTES;
+  static constexpr int OFF_RING = OFF_V + KV_BYTES;
   static constexpr int SMEM_BYTES = OFF_RING + NST * UNIT_BYTES + 1024;
   static constexpr uint32_t TM_ST = 0, TM_DPT = 2 * BQ, TM_DV = 4 * BQ, TM_DK = 4 * BQ + D, TM_COLS = 512;
 };
 
 struct DkvSmemCtl {
   uint64_t kv_full;
-  uint64_t ring_full[4], ring_empty[4];
-  uint64_t st_full[2], st_empty[2], pt_full[2], pt_done[2];
-  uint64_t drain;
-  float lse2[4][64];
-  float delta[4][64];
+  uint64_t ring_full[8], ring_empty[8];
+  uint64_t st_full[2], pt_full[2];
+  uint64_t acc_done, drain;
+  alignas(16) float lse2[8][64];  // read as float4
+  alignas(16) float delta[8][64];
+  int32_t qpos0[8], qrows[8];
   uint32_t tmem_base;
   int abort_flag;
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const DkvArgs a) {
   using C = DkvCfg<D>;
@@ -353,8 +369,6 @@ __global__ void __launch_bounds__(192, 1)
   __shared__ DkvSmemCtl ctl;
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
-  uint8_t* sPT = smem + C::OFF_PT;
-  uint8_t* sDST = smem + C::OFF_DST;
   uint8_t* sRing = smem + C::OFF_RING;
 
   const KVTileItem it = a.items[blockIdx.x];
@@ -367,15 +381,14 @@ __global__ void __launch_bounds__(192, 1)
     ctl.abort_flag = 0;
     mbar_init(&ctl.kv_full, 1);
     for (int i = 0; i < C::NST; ++i) {
-      mbar_init(&ctl.ring_full[i], 33);  // expect_tx arrival + 32 lanes after their lse/delta stores
+      mbar_init(&ctl.ring_full[i], 33);  // expect_tx arrival + 32 lanes after their smem stores
       mbar_init(&ctl.ring_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl.st_full[i], 1);
-      mbar_init(&ctl.st_empty[i], 4);
-      mbar_init(&ctl.pt_full[i], 4);
-      mbar_init(&ctl.pt_done[i], 1);
+      mbar_init(&ctl.pt_full[i], 8);
     }
+    mbar_init(&ctl.acc_done, 1);
     mbar_init(&ctl.drain, 1);
     fence_mbar_init();
   }
@@ -389,7 +402,10 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t tmem = ctl.tmem_base;
 
   if (warp == 0) {
-    // producer (whole warp): K, V tiles once; then per query block Q, dO (TMA) and lse2, Delta
+    // producer (whole warp): K, V tiles once; per query block Q, dO (TMA) and its
+    // lse2, Delta, position.  The next block's descriptor and per-row values are
+    // loaded into registers before waiting for its ring slot, so only the TMA
+    // latency remains between a slot being freed and refilled.
     bool ok = true;
     int i = 0;
     if (n_iter > 0) {
@@ -400,13 +416,27 @@ __global__ void __launch_bounds__(192, 1)
           tma_load_3d(sV + c * C::BN * 128, &tmV, &ctl.kv_full, c * 64, it.kv_head, it.k_row0);
         }
       }
+      // values of block i, fetched one iteration ahead
+      auto fetch = [&](int idx, int& h, QBlock& qb, float (&l2)[2], float (&dl)[2]) {
+        const int itx = it.it_lo + idx;
+        h = it.kv_head * gs + itx / it.list_len;
+        qb = a.qblocks[it.list_begin + itx % it.list_len];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int c = (int)lane + 32 * e;
+          const bool v = c < qb.q_rows;
+          const int64_t rix = (int64_t)h * a.T + qb.q_row0 + c;
+          l2[e] = v ? a.lse2[rix] : INFINITY;
+          dl[e] = v ? a.delta[rix] : 0.f;
+        }
+      };
+      int h;
+      QBlock qb;
+      float l2[2], dl[2];
+      fetch(0, h, qb, l2, dl);
       for (; i < n_iter; ++i) {
-        const int itx = it.it_lo + i;
-        const int h = it.kv_head * gs + itx / it.list_len;
-        const QBlock qb = a.qblocks[it.list_begin + itx % it.list_len];
         const int slot = i % C::NST;
-        const uint32_t ph = (i / C::NST) & 1;
-        if (!(ok = mbar_wait(&ctl.ring_empty[slot], ph ^ 1, fs))) break;
+        if (!(ok = mbar_wait(&ctl.ring_empty[slot], ((i / C::NST) & 1) ^ 1, fs))) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(&ctl.ring_full[slot], C::UNIT_BYTES);
           uint8_t* dst = sRing + slot * C::UNIT_BYTES;
@@ -414,14 +444,16 @@ __global__ void __launch_bounds__(192, 1)
             tma_load_3d(dst + c * C::BQ * 128, &tmQ, &ctl.ring_full[slot], c * 64, h, qb.q_row0);
             tma_load_3d(dst + C::QB_BYTES + c * C::BQ * 128, &tmDO, &ctl.ring_full[slot], c * 64, h, qb.q_row0);
           }
+          ctl.qpos0[slot] = qb.q_pos0;
+          ctl.qrows[slot] = qb.q_rows;
         }
-        for (int c = (int)lane; c < C::BQ; c += 32) {
-          const bool v = c < qb.q_rows;
-          const int64_t rix = (int64_t)h * a.T + qb.q_row0 + c;
-          ctl.lse2[slot][c] = v ? a.lse2[rix] : INFINITY;
-          ctl.delta[slot][c] = v ? a.delta[rix] : 0.f;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          ctl.lse2[slot][lane + 32 * e] = l2[e];
+          ctl.delta[slot][lane + 32 * e] = dl[e];
         }
         mbar_arrive(&ctl.ring_full[slot]);
+        if (i + 1 < n_iter) fetch(i + 1, h, qb, l2, dl);
       }
       if (!ok && lane == 0) {
         mbar_wait_drain(&ctl.kv_full, 0, kWaitLimitNs);
@@ -432,58 +464,71 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
   } else if (warp == 1) {
-    // MMA issuer
-    if (lane == 0 && n_iter > 0) {
+    // MMA issuer: S^T_i = K Q_i^T, dP^T_i = V dO_i^T (SS, N = 64); then
+    // dV += P^T_{i-1} dO_{i-1}, dK += dS^T_{i-1} Q_{i-1} (TS, N = D).  The whole
+    // warp runs the loop (warp-uniform descriptors); one elected lane issues.
+    if (n_iter > 0) {
       constexpr uint32_t idST = idesc_bf16(128, C::BQ, 0, 0);
       constexpr uint32_t idKV = idesc_bf16(128, D, 0, 1);
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aPT = smem_u32(sPT), aDST = smem_u32(sDST),
-                     aRing = smem_u32(sRing);
+      const uint64_t kdesc = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t vdesc = sdesc_sw128(smem_u32(sV), 16, 1024);
+      const uint32_t aRing = smem_u32(sRing);
       bool ok = mbar_wait(&ctl.kv_full, 0, fs);
       tc_fence_after();
       for (int i = 0; i <= n_iter && ok; ++i) {
         if (i < n_iter) {
-          const int b = i & 1, slot = i % C::NST;
-          if (!(ok = mbar_wait(&ctl.st_empty[b], ((i >> 1) & 1) ^ 1, fs))) break;
+          const uint32_t b = i & 1;
+          const int slot = i % C::NST;
           if (!(ok = mbar_wait(&ctl.ring_full[slot], (i / C::NST) & 1, fs))) break;
           tc_fence_after();
-          const uint32_t qb = aRing + slot * C::UNIT_BYTES, dob = qb + C::QB_BYTES;
+          const uint64_t qd = sdesc_sw128(aRing + slot * C::UNIT_BYTES, 16, 1024);
+          const uint64_t dod = sdesc_add(qd, C::QB_BYTES);
+          const uint32_t tS = tmem + C::TM_ST + b * C::BQ, tP = tmem + C::TM_DPT + b * C::BQ;
+          if (elect_one()) {
 #pragma unroll
-          for (int c = 0; c < C::KCH; ++c)
+            for (int c = 0; c < C::KCH; ++c)
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_bf16_ss(tmem + C::TM_ST + b * C::BQ, sdesc_sw128(aK + c * C::BN * 128 + k * 32, 16, 1024),
-                          sdesc_sw128(qb + c * C::BQ * 128 + k * 32, 16, 1024), idST, (c | k) != 0);
-#pragma unroll
-          for (int c = 0; c < C::KCH; ++c)
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_bf16_ss(tmem + C::TM_DPT + b * C::BQ, sdesc_sw128(aV + c * C::BN * 128 + k * 32, 16, 1024),
-                          sdesc_sw128(dob + c * C::BQ * 128 + k * 32, 16, 1024), idST, (c | k) != 0);
-          mma_commit(&ctl.st_full[b]);
+              for (int k = 0; k < 4; ++k) {
+                mma_bf16_ss(tS, sdesc_add(kdesc, c * C::BN * 128 + k * 32), sdesc_add(qd, c * C::BQ * 128 + k * 32),
+                            idST, (c | k) != 0);
+                mma_bf16_ss(tP, sdesc_add(vdesc, c * C::BN * 128 + k * 32), sdesc_add(dod, c * C::BQ * 128 + k * 32),
+                            idST, (c | k) != 0);
+              }
+            mma_commit(&ctl.st_full[b]);
+          }
+          __syncwarp();
         }
         if (i >= 1) {
-          const int ii = i - 1, b = ii & 1, slot = ii % C::NST;
+          const int ii = i - 1, slot = ii % C::NST;
+          const uint32_t b = ii & 1;
           if (!(ok = mbar_wait(&ctl.pt_full[b], (ii >> 1) & 1, fs))) break;
           tc_fence_after();
-          const uint32_t qb = aRing + slot * C::UNIT_BYTES, dob = qb + C::QB_BYTES;
+          const uint64_t qmn = sdesc_sw128(aRing + slot * C::UNIT_BYTES, C::BQ * 128, 1024);
+          const uint64_t domn = sdesc_add(qmn, C::QB_BYTES);
+          const uint32_t tPT = tmem + C::TM_ST + b * C::BQ, tDST = tmem + C::TM_DPT + b * C::BQ;
+          const uint32_t acc0 = ii > 0 ? 1u : 0u;
+          if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < C::BQ / 16; ++k) {
-            const uint32_t acc = (ii > 0 || k > 0) ? 1u : 0u;
-            mma_bf16_ss(tmem + C::TM_DV, sdesc_sw128(aPT + b * C::PT_BYTES + k * 32, 16, 1024),
-                        sdesc_sw128(dob + k * 16 * 128, C::BQ * 128, 1024), idKV, acc);
-            mma_bf16_ss(tmem + C::TM_DK, sdesc_sw128(aDST + b * C::PT_BYTES + k * 32, 16, 1024),
-                        sdesc_sw128(qb + k * 16 * 128, C::BQ * 128, 1024), idKV, acc);
+            for (int k = 0; k < C::BQ / 16; ++k) {
+              const uint32_t acc = k > 0 ? 1u : acc0;
+              mma_bf16_ts(tmem + C::TM_DV, tPT + packed_kstep_col(k), sdesc_add(domn, k * 16 * 128), idKV, acc);
+              mma_bf16_ts(tmem + C::TM_DK, tDST + packed_kstep_col(k), sdesc_add(qmn, k * 16 * 128), idKV, acc);
+            }
+            mma_commit(&ctl.ring_empty[slot]);
           }
-          mma_commit(&ctl.ring_empty[slot]);
-          mma_commit(&ctl.pt_done[b]);
+          __syncwarp();
         }
       }
-      mma_commit(&ctl.drain);
+      if (elect_one()) {
+        if (ok) mma_commit(&ctl.acc_done);
+        mma_commit(&ctl.drain);
+      }
+      __syncwarp();
       mbar_wait_drain(&ctl.drain, 0, kWaitLimitNs);
     }
   } else {
-    // P^T / dS^T warps: thread <-> key row
-    const uint32_t wq = warp & 3;
+    // compute warps: thread <-> key row, half <-> 32 query columns of each 64-query block
+    const uint32_t wq = warp & 3, half = (warp - 2) >> 2;
     const int row = (int)(wq * 32 + lane);
     const uint32_t tl = tmem + ((wq * 32) << 16);
     const int kpos = it.k_pos0 + row;
@@ -491,58 +536,56 @@ __global__ void __launch_bounds__(192, 1)
     const float sl2 = a.scale_log2;
     bool ok = true;
     for (int i = 0; i < n_iter; ++i) {
-      const int b = i & 1, slot = i % C::NST;
-      const int itx = it.it_lo + i;
-      const QBlock qb = a.qblocks[it.list_begin + itx % it.list_len];
+      const uint32_t b = i & 1;
+      const int slot = i % C::NST;
       if (!(ok = mbar_wait(&ctl.st_full[b], (i >> 1) & 1, fs))) break;
-      tc_fence_after();
-      // allowed query columns [clo, chi]: q_pos >= k_pos and (window) q_pos - k_pos < window
-      int clo = kpos - qb.q_pos0;
-      int chi = qb.q_rows - 1;
-      if (a.window > 0) chi = min(chi, kpos + a.window - 1 - qb.q_pos0);
-      if (!kvalid) chi = -1;
-      uint32_t sr[64], dr[64];
-      tmem_ld32(tl + C::TM_ST + b * C::BQ, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(tl + C::TM_ST + b * C::BQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_ld32(tl + C::TM_DPT + b * C::BQ, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
-      tmem_ld32(tl + C::TM_DPT + b * C::BQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.st_empty[b]);
-      if (i >= 2 && !(ok = mbar_wait(&ctl.pt_done[b], ((i - 2) >> 1) & 1, fs))) break;
-      // acquire the producer's lse2/delta stores for this block; the slot cannot
-      // be refilled before this block's dV/dK MMAs complete, so its phase is current
+      // acquire the producer's smem stores of this block (the slot's phase is current:
+      // it cannot be refilled before this block's dV/dK MMAs complete)
       if (!(ok = mbar_wait(&ctl.ring_full[slot], (i / C::NST) & 1, fs))) break;
-      const float* L2 = ctl.lse2[slot];
-      const float* DL = ctl.delta[slot];
-      const uint32_t pb = smem_u32(sPT + b * C::PT_BYTES), sb = smem_u32(sDST + b * C::PT_BYTES);
+      tc_fence_after();
+      const int qpos0 = ctl.qpos0[slot] + 32 * (int)half;
+      const int qrows = ctl.qrows[slot] - 32 * (int)half;
+      // allowed query columns [clo, chi] of this half: q_pos >= k_pos, q_pos - k_pos < window
+      const int clo = kpos - qpos0;
+      int chi = qrows - 1;
+      if (a.window > 0) chi = min(chi, kpos + a.window - 1 - qpos0);
+      if (!kvalid) chi = -1;
+      const bool full = (clo <= 0) && (chi >= 31);
+      uint32_t sr[32], dr[32];
+      tmem_ld32(tl + C::TM_ST + b * C::BQ + 32 * half, sr);
+      tmem_ld32(tl + C::TM_DPT + b * C::BQ + 32 * half, dr);
+      const float4* L4 = reinterpret_cast<const float4*>(&ctl.lse2[slot][32 * half]);
+      const float4* D4 = reinterpret_cast<const float4*>(&ctl.delta[slot][32 * half]);
+      tmem_ld_wait();
+      uint32_t wp[16], ws[16];
 #pragma unroll
-      for (int pc = 0; pc < 8; ++pc) {
-        uint32_t wp[4], ws[4];
+      for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 l4 = L4[e4], d4 = D4[e4];
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = pc * 8 + e * 2;
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -L2[c]));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, -L2[c + 1]));
-          p0 = (c < clo || c > chi) ? 0.f : p0;
-          p1 = (c + 1 < clo || c + 1 > chi) ? 0.f : p1;
-          const float d0 = p0 * (__uint_as_float(dr[c]) - DL[c]);
-          const float d1 = p1 * (__uint_as_float(dr[c + 1]) - DL[c + 1]);
-          wp[e] = pack_bf16x2(p0, p1);
-          ws[e] = pack_bf16x2(d0, d1);
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int c = 4 * e4 + 2 * e2;
+          float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lv[2 * e2]));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, -lv[2 * e2 + 1]));
+          if (!full) {
+            p0 = (c < clo || c > chi) ? 0.f : p0;
+            p1 = (c + 1 < clo || c + 1 > chi) ? 0.f : p1;
+          }
+          wp[2 * e4 + e2] = pack_bf16x2(p0, p1);
+          ws[2 * e4 + e2] = pack_bf16x2(p0 * (__uint_as_float(dr[c]) - dv[2 * e2]),
+                                        p1 * (__uint_as_float(dr[c + 1]) - dv[2 * e2 + 1]));
         }
-        st_shared_v4(pb + sw128_offset(row, pc), wp[0], wp[1], wp[2], wp[3]);
-        st_shared_v4(sb + sw128_offset(row, pc), ws[0], ws[1], ws[2], ws[3]);
       }
-      fence_proxy_async_smem();
+      tmem_st16(tl + C::TM_ST + b * C::BQ + 32 * half, wp);
+      tmem_st16(tl + C::TM_DPT + b * C::BQ + 32 * half, ws);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.pt_full[b]);
     }
     if (ok) {
       if (n_iter > 0) {
-        ok = mbar_wait(&ctl.pt_done[(n_iter - 1) & 1], ((n_iter - 1) >> 1) & 1, fs);
+        ok = mbar_wait(&ctl.acc_done, 0, fs);
         tc_fence_after();
       }
       if (ok) {
@@ -553,10 +596,11 @@ __global__ void __launch_bounds__(192, 1)
         for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK
           const float mul = which ? a.scale : 1.f;
 #pragma unroll
-          for (int c4 = 0; c4 < D / 32; ++c4) {
+          for (int c4 = 0; c4 < D / 64; ++c4) {
+            const int col = (int)half * (D / 2) + c4 * 32;
             uint32_t rr[32];
             if (n_iter > 0) {
-              tmem_ld32(tl + (which ? C::TM_DK : C::TM_DV) + c4 * 32, rr);
+              tmem_ld32(tl + (which ? C::TM_DK : C::TM_DV) + col, rr);
               tmem_ld_wait();
             } else {
 #pragma unroll
@@ -564,7 +608,7 @@ __global__ void __launch_bounds__(192, 1)
             }
             if (!kvalid) continue;
             if (pk) {
-              float4* dst = reinterpret_cast<float4*>((which ? pk : pv) + c4 * 32);
+              float4* dst = reinterpret_cast<float4*>((which ? pk : pv) + col);
 #pragma unroll
               for (int v = 0; v < 8; ++v)
                 dst[v] = make_float4(__uint_as_float(rr[4 * v]) * mul, __uint_as_float(rr[4 * v + 1]) * mul,
@@ -574,7 +618,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
               for (int e = 0; e < 16; ++e)
                 w[e] = pack_bf16x2(__uint_as_float(rr[2 * e]) * mul, __uint_as_float(rr[2 * e + 1]) * mul);
-              uint4* dst = reinterpret_cast<uint4*>((which ? a.dk : a.dv) + orow + c4 * 32);
+              uint4* dst = reinterpret_cast<uint4*>((which ? a.dk : a.dv) + orow + col);
 #pragma unroll
               for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
             }
@@ -669,7 +713,7 @@ static cudaError_t launch_tc(K kernel, const CUtensorMap& t0, const CUtensorMap&
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kernel<<<n_items, 192, Cfg::SMEM_BYTES, st>>>(t0, t1, t2, t3, a);
+  kernel<<<n_items, kBwdThreads, Cfg::SMEM_BYTES, st>>>(t0, t1, t2, t3, a);
   return cudaGetLastError();
 }
 

@@ -179,6 +179,16 @@ def sample_response_keys(w, rng, n_random=6):
     return sorted(keys)
 
 
+def attended_keys(w, row):
+    off = w.offsets
+    if row < w.P:
+        pos = row
+    else:
+        n = max(i for i in range(w.N) if w.P + off[i] <= row and off[i + 1] > off[i])
+        pos = w.P + row - (w.P + off[n])
+    return pos + 1 if w.window <= 0 else min(pos + 1, w.window)
+
+
 def groups_to_check(w, rng):
     return sorted({int(rng.integers(0, w.Hkv)), w.Hkv - 1})
 
@@ -204,6 +214,12 @@ def check_sampled(w, q, k, v, do, g, prompt_keys=False):
             assert relF(dq_g[:nu], dq_r[:nu]) <= G_REL
             rms_row = np.linalg.norm(dq_r[:nu]) / math.sqrt(nu)
             for i in range(nu, len(rows)):
+                # a row attending only a handful of keys (the first prompt rows) carries the
+                # inherent error of Delta computed on the bf16 output, |dDelta| ~ 2^-9 |dO o O|,
+                # which is of the order of its own tiny-key dQ; such rows are compared in the
+                # small full-oracle cases instead
+                if attended_keys(w, rows[i]) < 64:
+                    continue
                 assert np.linalg.norm(dq_g[i] - dq_r[i]) <= G_REL * max(rms_row, np.linalg.norm(dq_r[i])), rows[i]
         keys = sample_response_keys(w, rng)
         if prompt_keys and w.P > 0:
