@@ -82,26 +82,34 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepArgs a) {
 constexpr int kBwdThreads = 320;
 
 __device__ __forceinline__ uint32_t packed_kstep_col(int k) { return 32u * (k >> 1) + 8u * (k & 1); }
+// The same for halves of 64 values (the dQ kernel's 128-key tiles): half h
+// writes its 32 packed columns at [64h, 64h+32), so K-step k (16 keys) sits at
+// column 64 (k / 4) + 8 (k % 4).
+__device__ __forceinline__ uint32_t packed_kstep_col64(int k) { return 64u * (k >> 2) + 8u * (k & 3); }
 
 // ---------------------------------------------------------------- dQ
+// 128-key tiles: S and dP are M=128 x N=128 MMAs.  S is double-buffered (its
+// buffer also carries dS to the dQ GEMM); dP is single-buffered and released
+// as soon as the compute warps have loaded it.  Each compute thread handles 64
+// key columns of its query row.  TMEM: S 2 x 128, dP 128, dQ D columns.
 template <int D>
 struct DqCfg {
-  static constexpr int BM = 128, BN = 64;
+  static constexpr int BM = 128, BN = 128;
   static constexpr int KCH = D / 64;
   static constexpr int Q_BYTES = BM * D * 2;         // Q and dO tiles (resident)
   static constexpr int TILE_BYTES = BN * D * 2;      // one K or V tile
-  static constexpr int NST = (D == 128) ? 10 : 16;
+  static constexpr int NST = (D == 128) ? 5 : 10;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = OFF_Q + Q_BYTES;
   static constexpr int OFF_RING = OFF_DO + Q_BYTES;
   static constexpr int SMEM_BYTES = OFF_RING + NST * TILE_BYTES + 1024;
-  static constexpr uint32_t TM_S = 0, TM_DP = 2 * BN, TM_DQ = 4 * BN, TM_COLS = 512;
+  static constexpr uint32_t TM_S = 0, TM_DP = 2 * BN, TM_DQ = 3 * BN, TM_COLS = 512;
 };
 
 struct DqSmemCtl {
   uint64_t q_full;
-  uint64_t ring_full[16], ring_empty[16];
-  uint64_t s_full[2], ds_full[2];
+  uint64_t ring_full[10], ring_empty[10];
+  uint64_t s_full[2], ds_full[2], dp_empty;
   uint64_t acc_done, drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -147,6 +155,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&ctl.s_full[i], 1);
       mbar_init(&ctl.ds_full[i], 8);
     }
+    mbar_init(&ctl.dp_empty, 8);
     mbar_init(&ctl.acc_done, 1);
     mbar_init(&ctl.drain, 1);
     fence_mbar_init();
@@ -192,7 +201,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // MMA issuer: S_j = Q K_j^T, dP_j = dO V_j^T (SS, N = 64), then dQ += dS_{j-1} K_{j-1} (TS, N = D).
+    // MMA issuer: S_j = Q K_j^T, dP_j = dO V_j^T (SS, N = 128), then dQ += dS_{j-1} K_{j-1} (TS, N = D).
     // The whole warp runs the loop so descriptors stay warp-uniform; one elected
     // lane issues each batch of MMAs and its commits.
     if (nt > 0) {
@@ -208,21 +217,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint32_t b = j & 1;
           const int ik = 2 * j, iv = 2 * j + 1;
           if (!(ok = mbar_wait(&ctl.ring_full[ik % C::NST], (ik / C::NST) & 1, fs))) break;
-          if (!(ok = mbar_wait(&ctl.ring_full[iv % C::NST], (iv / C::NST) & 1, fs))) break;
           tc_fence_after();
           const uint64_t kd = sdesc_sw128(aRing + (ik % C::NST) * C::TILE_BYTES, 16, 1024);
-          const uint64_t vd = sdesc_sw128(aRing + (iv % C::NST) * C::TILE_BYTES, 16, 1024);
-          const uint32_t tS = tmem + C::TM_S + b * C::BN, tP = tmem + C::TM_DP + b * C::BN;
+          const uint32_t tS = tmem + C::TM_S + b * C::BN;
           if (elect_one()) {
 #pragma unroll
             for (int c = 0; c < C::KCH; ++c)
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
+              for (int k = 0; k < 4; ++k)
                 mma_bf16_ss(tS, sdesc_add(dQd, c * C::BM * 128 + k * 32), sdesc_add(kd, c * C::BN * 128 + k * 32),
                             idS, (c | k) != 0);
-                mma_bf16_ss(tP, sdesc_add(dDOd, c * C::BM * 128 + k * 32), sdesc_add(vd, c * C::BN * 128 + k * 32),
-                            idS, (c | k) != 0);
-              }
+          }
+          __syncwarp();
+          // dP has one buffer: the compute warps must have loaded dP_{j-1}
+          if (!(ok = mbar_wait(&ctl.ring_full[iv % C::NST], (iv / C::NST) & 1, fs))) break;
+          if (j >= 1 && !(ok = mbar_wait(&ctl.dp_empty, (j - 1) & 1, fs))) break;
+          tc_fence_after();
+          const uint64_t vd = sdesc_sw128(aRing + (iv % C::NST) * C::TILE_BYTES, 16, 1024);
+          if (elect_one()) {
+#pragma unroll
+            for (int c = 0; c < C::KCH; ++c)
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_bf16_ss(tmem + C::TM_DP, sdesc_add(dDOd, c * C::BM * 128 + k * 32),
+                            sdesc_add(vd, c * C::BN * 128 + k * 32), idS, (c | k) != 0);
             mma_commit(&ctl.ring_empty[iv % C::NST]);
             mma_commit(&ctl.s_full[b]);
           }
@@ -239,7 +257,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (elect_one()) {
 #pragma unroll
             for (int k = 0; k < C::BN / 16; ++k)
-              mma_bf16_ts(tmem + C::TM_DQ, tA + packed_kstep_col(k), sdesc_add(kmn, k * 16 * 128), idQ,
+              mma_bf16_ts(tmem + C::TM_DQ, tA + packed_kstep_col64(k), sdesc_add(kmn, k * 16 * 128), idQ,
                           k > 0 ? 1u : acc0);
             mma_commit(&ctl.ring_empty[ik % C::NST]);
           }
@@ -254,7 +272,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_wait_drain(&ctl.drain, 0, kWaitLimitNs);
     }
   } else {
-    // compute warps: thread <-> query row, half <-> 32 key columns of each 64-key block
+    // compute warps: thread <-> query row, half <-> 64 key columns of each 128-key tile
     const uint32_t wq = warp & 3, half = (warp - 2) >> 2;
     const int row = (int)(wq * 32 + lane);
     const uint32_t tl = tmem + ((wq * 32) << 16);
@@ -270,21 +288,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int r, t;
       qtile_of(it, j, r, t);
       const KeyRegion& kr = it.reg[r];
-      const int kl0 = t * C::BN + 32 * (int)half;
+      const int kl0 = t * C::BN + 64 * (int)half;
       int lo = 0;
       if (a.window > 0) lo = max(0, qpos - a.window + 1 - kr.pos0);
       const int hi = min(kr.count - 1, qpos - kr.pos0);
       const int clo = lo - kl0, chi = hi - kl0;  // allowed columns of this half
-      const bool full = (clo <= 0) && (chi >= 31);
+      const bool full = (clo <= 0) && (chi >= 63);
       if (!(ok = mbar_wait(&ctl.s_full[b], (j >> 1) & 1, fs))) break;
       tc_fence_after();
-      uint32_t sr[32], dr[32];
-      tmem_ld32(tl + C::TM_S + b * C::BN + 32 * half, sr);
-      tmem_ld32(tl + C::TM_DP + b * C::BN + 32 * half, dr);
+      uint32_t sr[64], dr[64];
+      tmem_ld32(tl + C::TM_S + b * C::BN + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+      tmem_ld32(tl + C::TM_S + b * C::BN + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+      tmem_ld32(tl + C::TM_DP + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
+      tmem_ld32(tl + C::TM_DP + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
       tmem_ld_wait();
-      uint32_t w[16];
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.dp_empty);
+      uint32_t w[32];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
+      for (int e = 0; e < 32; ++e) {
         const int c = 2 * e;
         float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2));
         float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, -lse2));
@@ -294,7 +317,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         w[e] = pack_bf16x2(p0 * (__uint_as_float(dr[c]) - delta), p1 * (__uint_as_float(dr[c + 1]) - delta));
       }
-      tmem_st16(tl + C::TM_S + b * C::BN + 32 * half, w);
+      tmem_st32(tl + C::TM_S + b * C::BN + 64 * half, w);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -677,7 +700,7 @@ cudaError_t launch_selftest_timeout(uint64_t limit_ns, uint32_t* status, cudaStr
 }
 
 int dq_query_tile(int /*D*/) { return 128; }
-int dq_key_tile(int /*D*/) { return 64; }
+int dq_key_tile(int /*D*/) { return 128; }
 int dkv_key_tile(int /*D*/) { return 128; }
 int dkv_query_block(int /*D*/) { return 64; }
 

@@ -159,10 +159,14 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && nt > 0) {
+    // The whole warp runs the loop so descriptors stay warp-uniform; one
+    // elected lane issues each batch of MMAs and its commits.
+    if (nt > 0) {
       constexpr uint32_t idS = idesc_bf16(128, C::BN, 0, 0);
       constexpr uint32_t idO = idesc_bf16(128, D, 0, 1);
-      const uint32_t aQ = smem_u32(sQ), aP = smem_u32(sP), aRing = smem_u32(sRing);
+      const uint64_t qdesc = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t pdesc = sdesc_sw128(smem_u32(sP), 16, 1024);
+      const uint32_t aRing = smem_u32(sRing);
       int slot = 0;
       uint32_t phase = 0;
       bool ok = mbar_wait(&ctl.q_full, 0, fs);
@@ -173,17 +177,19 @@ __global__ void __launch_bounds__(192, 1)
           if (!(ok = mbar_wait(&ctl.s_empty[b], ((j >> 1) & 1) ^ 1, fs))) break;
           if (!(ok = mbar_wait(&ctl.ring_full[slot], phase, fs))) break;
           tc_fence_after();
-          const uint32_t kbase = aRing + slot * C::TILE_BYTES;
+          const uint64_t kdesc = sdesc_sw128(aRing + slot * C::TILE_BYTES, 16, 1024);
+          const uint32_t tS = tmem + C::TM_S + b * C::BN;
+          if (elect_one()) {
 #pragma unroll
-          for (int c = 0; c < C::KCH; ++c)
+            for (int c = 0; c < C::KCH; ++c)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t ad = sdesc_sw128(aQ + c * C::BM * 128 + k * 32, 16, 1024);
-              const uint64_t bd = sdesc_sw128(kbase + c * C::BN * 128 + k * 32, 16, 1024);
-              mma_bf16_ss(tmem + C::TM_S + b * C::BN, ad, bd, idS, (c | k) != 0);
-            }
-          mma_commit(&ctl.ring_empty[slot]);
-          mma_commit(&ctl.s_full[b]);
+              for (int k = 0; k < 4; ++k)
+                mma_bf16_ss(tS, sdesc_add(qdesc, c * C::BM * 128 + k * 32), sdesc_add(kdesc, c * C::BN * 128 + k * 32),
+                            idS, (c | k) != 0);
+            mma_commit(&ctl.ring_empty[slot]);
+            mma_commit(&ctl.s_full[b]);
+          }
+          __syncwarp();
           if (++slot == C::NST) {
             slot = 0;
             phase ^= 1;
@@ -194,16 +200,18 @@ __global__ void __launch_bounds__(192, 1)
           if (!(ok = mbar_wait(&ctl.p_full[b], (jj >> 1) & 1, fs))) break;
           if (!(ok = mbar_wait(&ctl.ring_full[slot], phase, fs))) break;
           tc_fence_after();
-          const uint32_t vbase = aRing + slot * C::TILE_BYTES;
-          const uint32_t pbase = aP + b * C::P_BYTES;
+          const uint64_t vdesc = sdesc_sw128(aRing + slot * C::TILE_BYTES, C::BN * 128, 1024);
+          const uint64_t pb = sdesc_add(pdesc, b * C::P_BYTES);
+          const uint32_t acc0 = jj > 0 ? 1u : 0u;
+          if (elect_one()) {
 #pragma unroll
-          for (int k = 0; k < C::BN / 16; ++k) {
-            const uint64_t ad = sdesc_sw128(pbase + (k >> 2) * C::BM * 128 + (k & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(vbase + k * 16 * 128, C::BN * 128, 1024);
-            mma_bf16_ss(tmem + C::TM_O, ad, bd, idO, (jj > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < C::BN / 16; ++k)
+              mma_bf16_ss(tmem + C::TM_O, sdesc_add(pb, (k >> 2) * C::BM * 128 + (k & 3) * 32),
+                          sdesc_add(vdesc, k * 16 * 128), idO, k > 0 ? 1u : acc0);
+            mma_commit(&ctl.ring_empty[slot]);
+            mma_commit(&ctl.pv_done[b]);
           }
-          mma_commit(&ctl.ring_empty[slot]);
-          mma_commit(&ctl.pv_done[b]);
+          __syncwarp();
           if (++slot == C::NST) {
             slot = 0;
             phase ^= 1;
@@ -211,7 +219,8 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       // every MMA issued above must finish before TMEM is released
-      mma_commit(&ctl.drain);
+      if (elect_one()) mma_commit(&ctl.drain);
+      __syncwarp();
       mbar_wait_drain(&ctl.drain, 0, kWaitLimitNs);
     }
   } else {
