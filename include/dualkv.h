@@ -153,6 +153,33 @@ int dualkv_profile_enable(int on);
 int dualkv_profile_read(double* ms, int64_t* launches);
 
 /*
+ * Backward pass that allocates no device memory.  The paper has no counterpart
+ * to this entry point: it is here for callers that cannot call cudaMalloc on
+ * the call path -- for example a runtime that hands all device memory to its
+ * own pool at start-up and fails any later allocation, or a host binding that
+ * owns no device allocator and holds only the buffers it was given.
+ *
+ * Same arguments and results as dualkv_bwd, without the workspace: Delta,
+ * the log2-scaled LSE, the split dK/dV partials, the work lists and a status
+ * word live in one fixed array of DUALKV_NOALLOC_SCRATCH_BYTES (32 MiB) in
+ * the library's device memory, which every GPU that loads the library holds
+ * until the process exits.  The first call on a device looks up that array's
+ * device address (set-up), so make that first call before any stream capture
+ * on the device.  A layout whose scratch would exceed the maximum is rejected
+ * with DUALKV_ERR_WORKSPACE before anything is launched.  Every call shares
+ * the array and leaves its contents behind; the status word is cleared at the
+ * start of each call and everything else is fully written before it is read.
+ * Calls that overlap on the GPU (different streams, or host threads) race on
+ * the array and corrupt each other's results.  The call returns after its
+ * kernels have finished on `stream`, with DUALKV_ERR_DEVICE if one of them
+ * reported a timed-out wait or an index out of range.
+ */
+#define DUALKV_NOALLOC_SCRATCH_BYTES 33554432
+int dualkv_bwd_noalloc(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                       const void* dout, int P, int N, const int32_t* R_offsets, int Hq, int Hkv, int D, float scale,
+                       int window, void* dq, void* dk, void* dv, void* stream);
+
+/*
  * Self-test of the kernels' failure path (no counterpart in the paper; it
  * exists so that timeout handling can be tested without faulting a GPU).
  * Launches one CTA of 64 threads that wait, with the same bounded mbarrier

@@ -30,7 +30,8 @@ DUALKV_ERR_UNSUPPORTED = 6
 # every symbol the header declares
 EXPORTS = ("dualkv_fwd", "dualkv_bwd_workspace_bytes", "dualkv_bwd", "dualkv_build_index", "dualkv_rho",
            "dualkv_pairs", "dualkv_check_status", "dualkv_error_string", "dualkv_profile_enable",
-           "dualkv_profile_read", "dualkv_selftest_timeout", "dualkv_release")
+           "dualkv_profile_read", "dualkv_selftest_timeout", "dualkv_bwd_noalloc", "dualkv_release")
+NOALLOC_SCRATCH_BYTES = 32 << 20
 KERNEL_KINDS = ("fwd", "prep", "dkv", "reduce", "dq")
 
 _lock = threading.Lock()
@@ -76,6 +77,8 @@ def load(path: Optional[str] = None):
         lib.dualkv_profile_enable.restype = ci
         lib.dualkv_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)]
         lib.dualkv_profile_read.restype = ci
+        lib.dualkv_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, i32p, ci, ci, ci, cf, ci, vp, vp, vp, vp]
+        lib.dualkv_bwd_noalloc.restype = ci
         lib.dualkv_selftest_timeout.argtypes = [ctypes.c_uint64, vp]
         lib.dualkv_selftest_timeout.restype = ci
         lib.dualkv_release.argtypes = []
@@ -148,6 +151,22 @@ def dualkv_bwd(q, k, v, out, lse, dout, P, N, R_offsets, Hq, Hkv, D, scale, wind
                            _offsets(R_offsets), int(Hq), int(Hkv), int(D), float(scale), int(window), _ptr(dq),
                            _ptr(dk), _ptr(dv), _ptr(workspace), int(workspace_bytes), _stream(stream))
     _raise(rc, "dualkv_bwd")
+
+
+def dualkv_bwd_noalloc(q, k, v, out, lse, dout, P, N, R_offsets, Hq, Hkv, D, scale, window, dq, dk, dv,
+                       stream=None) -> None:
+    """dualkv_bwd without a workspace: for callers that cannot allocate device
+    memory.  Its scratch is a fixed array inside the library (NOALLOC_SCRATCH_BYTES
+    per GPU); calls overlapping on the GPU race on it.  Returns once the pass has
+    finished on `stream`."""
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
+                        ("out", out, torch.bfloat16), ("lse", lse, torch.float32), ("dout", dout, torch.bfloat16),
+                        ("dq", dq, torch.bfloat16), ("dk", dk, torch.bfloat16), ("dv", dv, torch.bfloat16)):
+        _check_dev(name, t, dt)
+    rc = load().dualkv_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), int(P), int(N),
+                                   _offsets(R_offsets), int(Hq), int(Hkv), int(D), float(scale), int(window),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream))
+    _raise(rc, "dualkv_bwd_noalloc")
 
 
 def dualkv_build_index(P, N, R_offsets):
