@@ -194,7 +194,8 @@ WsLayout ws_layout(int64_t T, int Hq, int D, int nslots) {
   return w;
 }
 
-bool supported_d(int D) { return D == 64 || D == 128; }
+bool supported_d(int D) { return D == 64 || D == 128; }  // backward
+bool supported_fwd_d(int D) { return D == 64 || D == 128 || D == 512; }
 
 }  // namespace
 
@@ -206,7 +207,7 @@ int dualkv_fwd(const void* q, const void* k, const void* v, int P, int N, const 
   if (!(scale > 0.f) || !std::isfinite(scale)) return DUALKV_ERR_INVALID;
   if (!q || !k || !v || !out || !lse) return DUALKV_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse)) return DUALKV_ERR_ALIGN;
-  if (!supported_d(D)) return DUALKV_ERR_UNSUPPORTED;
+  if (!supported_fwd_d(D)) return DUALKV_ERR_UNSUPPORTED;
   const int64_t T = (int64_t)P + R_offsets[N];
   std::lock_guard<std::mutex> lock(g_mu);
   int rc = ensure_encode();

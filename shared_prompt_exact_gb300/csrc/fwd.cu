@@ -1,4 +1,4 @@
-// fwd.cu -- DualKV forward kernel for sm_103a (head dimension 64 / 128).
+// fwd.cu -- DualKV forward kernel for sm_103a (head dimension 64, 128, 512).
 //
 // DualKV paper, abstract: a fused forward kernel that iterates over two
 // disjoint KV regions -- the shared prompt and the query's own response
@@ -8,15 +8,24 @@
 // range, with an online softmax.
 //
 // Warp roles (192 threads):
-//   warp 0      TMA producer: Q tile once, then K and V tiles into a ring, in
-//               the order the MMA warp consumes them (K0, K1, V0, K2, V1, ...)
-//   warp 1      TMEM owner and MMA issuer (one thread): S_j = Q K_j^T into one
-//               of two TMEM S buffers, O += P_{j-1} V_{j-1} into the TMEM O
-//               accumulator
+//   warp 0      TMA producer: the Q tile once, then K and V tiles through a
+//               ring of "units" (128 rows x 128 head-dim columns, two 64-column
+//               TMA boxes) in the order the MMA warp consumes them
+//               (K_0, K_1, V_0, K_2, V_1, ...)
+//   warp 1      TMEM owner and MMA issuer (whole warp, one elected lane issues):
+//               S_j = Q K_j^T (A and B in shared memory) into one of two TMEM
+//               S buffers; O += P_{j-1} V_{j-1} with P read from TMEM
 //   warps 2-5   softmax: thread <-> query row (TMEM lane); reads S_j, masks,
-//               keeps the running max m and sum l, writes P_j (bf16) to shared
-//               memory, rescales O in TMEM when m grows by more than 2^8, and
-//               finally writes out = O / l and lse = m + ln l.
+//               keeps the running max m and sum l (log2 units), writes P_j as
+//               packed bf16 over the first 64 columns of S_j's own buffer,
+//               rescales O in TMEM when m grows by more than 2^8 (exact: O and
+//               l share the stale max), finally writes out = O / l and lse.
+// tcgen05.mma ops issued by one thread execute in issue order, so S_{j+2} is
+// written into the buffer holding P_j only after PV_j, which reads it.
+//
+// Head dimension 512: the 128 x 512 fp32 O accumulator would fill all of TMEM,
+// so the output columns are split over two CTAs (NSPLIT = 2, 256 columns each);
+// both compute the full S = Q K^T (contraction over all 512 columns).
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -29,25 +38,28 @@ namespace {
 template <int D>
 struct FwdCfg {
   static constexpr int BM = 128, BN = 128;
-  static constexpr int KCH = D / 64;                  // 64-column chunks of the head dimension
+  static constexpr int NSPLIT = (D == 512) ? 2 : 1;
+  static constexpr int DV = D / NSPLIT;                // output columns of one CTA
+  static constexpr int QCH = D / 64;                   // 64-column chunks of Q / K
+  static constexpr int UCH = (D == 64) ? 1 : 2;        // chunks per ring unit
+  static constexpr int UNIT_BYTES = UCH * BN * 128;    // 16 or 32 KB
+  static constexpr int KU = QCH / UCH;                 // units per K tile
+  static constexpr int VU = (DV / 64) / UCH;           // units per V tile (this CTA's columns)
   static constexpr int Q_BYTES = BM * D * 2;
-  static constexpr int TILE_BYTES = BN * D * 2;        // one K or V tile
-  static constexpr int P_BYTES = BM * BN * 2;
-  static constexpr int NST = (D == 128) ? 4 : 6;       // ring slots
+  static constexpr int NST = (D == 512) ? 3 : (D == 128 ? 6 : 12);
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_P = OFF_Q + Q_BYTES;
-  static constexpr int OFF_RING = OFF_P + 2 * P_BYTES;
-  static constexpr int SMEM_BYTES = OFF_RING + NST * TILE_BYTES + 1024;  // + alignment slack
+  static constexpr int OFF_RING = Q_BYTES;
+  static constexpr int SMEM_BYTES = OFF_RING + NST * UNIT_BYTES + 1024;  // + alignment slack
   static constexpr uint32_t TM_S = 0;                  // S buffers at columns 0 and BN
-  static constexpr uint32_t TM_O = 2 * BN;             // O accumulator
+  static constexpr uint32_t TM_O = 2 * BN;             // O accumulator (DV columns)
   static constexpr uint32_t TM_COLS = 512;
   static constexpr float RESCALE_THRESHOLD = 8.0f;     // log2 units
 };
 
 struct FwdSmemCtl {
   uint64_t q_full;
-  uint64_t ring_full[8], ring_empty[8];
-  uint64_t s_full[2], s_empty[2], p_full[2], pv_done[2];
+  uint64_t ring_full[12], ring_empty[12];
+  uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -73,10 +85,10 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ FwdSmemCtl ctl;
   uint8_t* sQ = smem + C::OFF_Q;
-  uint8_t* sP = smem + C::OFF_P;
   uint8_t* sRing = smem + C::OFF_RING;
 
-  const QTileItem it = a.items[blockIdx.x];
+  const QTileItem it = a.items[blockIdx.x / C::NSPLIT];
+  const int split = (int)(blockIdx.x % C::NSPLIT);
   const int nt0 = it.reg[0].t_hi - it.reg[0].t_lo;
   const int nt = nt0 + (it.reg[1].t_hi - it.reg[1].t_lo);
   const int kvh = it.head / (a.Hq / a.Hkv);
@@ -92,7 +104,6 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl.s_full[i], 1);
-      mbar_init(&ctl.s_empty[i], 4);
       mbar_init(&ctl.p_full[i], 4);
       mbar_init(&ctl.pv_done[i], 1);
     }
@@ -115,106 +126,94 @@ __global__ void __launch_bounds__(192, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       mbar_arrive_expect_tx(&ctl.q_full, C::Q_BYTES);
-      for (int c = 0; c < C::KCH; ++c)
+      for (int c = 0; c < C::QCH; ++c)
         tma_load_3d(sQ + c * C::BM * 128, &tmQ, &ctl.q_full, c * 64, it.head, it.q_row0);
-      int slot = 0;
-      uint32_t phase = 0;
-      int pushes = 0;
+      int idx = 0;
       bool ok = true;
+      // units in consumption order: K_0; then for j = 1..nt: K_j (if j < nt), V_{j-1}
       for (int j = 0; j <= nt && ok; ++j) {
         for (int kind = 0; kind < 2 && ok; ++kind) {
-          const int jj = kind == 0 ? j : j - 1;  // K_j then V_{j-1}
+          const int jj = kind == 0 ? j : j - 1;
           if (jj < 0 || jj >= nt) continue;
           int r, t;
           tile_of(it, jj, r, t);
           const int key_row = it.reg[r].row0 + t * C::BN;
-          if (!mbar_wait(&ctl.ring_empty[slot], phase ^ 1, fs)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&ctl.ring_full[slot], C::TILE_BYTES);
-          uint8_t* dst = sRing + slot * C::TILE_BYTES;
+          const int nu = kind == 0 ? C::KU : C::VU;
+          const int col0 = kind == 0 ? 0 : split * C::DV;
           const CUtensorMap* tm = kind == 0 ? &tmK : &tmV;
-          for (int c = 0; c < C::KCH; ++c) tma_load_3d(dst + c * C::BN * 128, tm, &ctl.ring_full[slot], c * 64, kvh, key_row);
-          ++pushes;
-          if (++slot == C::NST) {
-            slot = 0;
-            phase ^= 1;
+          for (int u = 0; u < nu; ++u, ++idx) {
+            const int slot = idx % C::NST;
+            if (!(ok = mbar_wait(&ctl.ring_empty[slot], ((idx / C::NST) & 1) ^ 1, fs))) break;
+            mbar_arrive_expect_tx(&ctl.ring_full[slot], C::UNIT_BYTES);
+            uint8_t* dst = sRing + slot * C::UNIT_BYTES;
+            for (int c = 0; c < C::UCH; ++c)
+              tma_load_3d(dst + c * C::BN * 128, tm, &ctl.ring_full[slot], col0 + (u * C::UCH + c) * 64, kvh, key_row);
           }
         }
       }
       if (!ok) {
         // drain: wait for every copy still in flight before the CTA can exit
         mbar_wait_drain(&ctl.q_full, 0, kWaitLimitNs);
-        for (int back = 1; back <= C::NST && back <= pushes; ++back) {
-          int s = slot - back;
-          uint32_t ph = phase;
-          if (s < 0) {
-            s += C::NST;
-            ph ^= 1;
-          }
-          mbar_wait_drain(&ctl.ring_full[s], ph, kWaitLimitNs);
+        for (int back = 1; back <= C::NST && back <= idx; ++back) {
+          const int i2 = idx - back;
+          mbar_wait_drain(&ctl.ring_full[i2 % C::NST], (i2 / C::NST) & 1, kWaitLimitNs);
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // The whole warp runs the loop so descriptors stay warp-uniform; one
-    // elected lane issues each batch of MMAs and its commits.
     if (nt > 0) {
       constexpr uint32_t idS = idesc_bf16(128, C::BN, 0, 0);
-      constexpr uint32_t idO = idesc_bf16(128, D, 0, 1);
+      constexpr uint32_t idO = idesc_bf16(128, C::UCH * 64, 0, 1);
       const uint64_t qdesc = sdesc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t pdesc = sdesc_sw128(smem_u32(sP), 16, 1024);
       const uint32_t aRing = smem_u32(sRing);
-      int slot = 0;
-      uint32_t phase = 0;
+      int idx = 0;
       bool ok = mbar_wait(&ctl.q_full, 0, fs);
       tc_fence_after();
       for (int j = 0; j <= nt && ok; ++j) {
         if (j < nt) {
-          const int b = j & 1;
-          if (!(ok = mbar_wait(&ctl.s_empty[b], ((j >> 1) & 1) ^ 1, fs))) break;
-          if (!(ok = mbar_wait(&ctl.ring_full[slot], phase, fs))) break;
-          tc_fence_after();
-          const uint64_t kdesc = sdesc_sw128(aRing + slot * C::TILE_BYTES, 16, 1024);
+          const uint32_t b = j & 1;
           const uint32_t tS = tmem + C::TM_S + b * C::BN;
-          if (elect_one()) {
+          for (int u = 0; u < C::KU && ok; ++u, ++idx) {
+            const int slot = idx % C::NST;
+            if (!(ok = mbar_wait(&ctl.ring_full[slot], (idx / C::NST) & 1, fs))) break;
+            tc_fence_after();
+            const uint64_t kdesc = sdesc_sw128(aRing + slot * C::UNIT_BYTES, 16, 1024);
+            const uint64_t qd = sdesc_add(qdesc, u * C::UCH * C::BM * 128);
+            if (elect_one()) {
 #pragma unroll
-            for (int c = 0; c < C::KCH; ++c)
+              for (int c = 0; c < C::UCH; ++c)
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                mma_bf16_ss(tS, sdesc_add(qdesc, c * C::BM * 128 + k * 32), sdesc_add(kdesc, c * C::BN * 128 + k * 32),
-                            idS, (c | k) != 0);
-            mma_commit(&ctl.ring_empty[slot]);
-            mma_commit(&ctl.s_full[b]);
+                for (int k = 0; k < 4; ++k)
+                  mma_bf16_ss(tS, sdesc_add(qd, c * C::BM * 128 + k * 32), sdesc_add(kdesc, c * C::BN * 128 + k * 32),
+                              idS, (u | c | k) != 0);
+              mma_commit(&ctl.ring_empty[slot]);
+              if (u == C::KU - 1) mma_commit(&ctl.s_full[b]);
+            }
+            __syncwarp();
           }
-          __syncwarp();
-          if (++slot == C::NST) {
-            slot = 0;
-            phase ^= 1;
-          }
+          if (!ok) break;
         }
         if (j >= 1) {
-          const int jj = j - 1, b = jj & 1;
+          const int jj = j - 1;
+          const uint32_t b = jj & 1;
           if (!(ok = mbar_wait(&ctl.p_full[b], (jj >> 1) & 1, fs))) break;
-          if (!(ok = mbar_wait(&ctl.ring_full[slot], phase, fs))) break;
-          tc_fence_after();
-          const uint64_t vdesc = sdesc_sw128(aRing + slot * C::TILE_BYTES, C::BN * 128, 1024);
-          const uint64_t pb = sdesc_add(pdesc, b * C::P_BYTES);
+          const uint32_t tP = tmem + C::TM_S + b * C::BN;
           const uint32_t acc0 = jj > 0 ? 1u : 0u;
-          if (elect_one()) {
+          for (int u = 0; u < C::VU && ok; ++u, ++idx) {
+            const int slot = idx % C::NST;
+            if (!(ok = mbar_wait(&ctl.ring_full[slot], (idx / C::NST) & 1, fs))) break;
+            tc_fence_after();
+            const uint64_t vdesc = sdesc_sw128(aRing + slot * C::UNIT_BYTES, C::BN * 128, 1024);
+            const uint32_t tO = tmem + C::TM_O + u * C::UCH * 64;
+            if (elect_one()) {
 #pragma unroll
-            for (int k = 0; k < C::BN / 16; ++k)
-              mma_bf16_ss(tmem + C::TM_O, sdesc_add(pb, (k >> 2) * C::BM * 128 + (k & 3) * 32),
-                          sdesc_add(vdesc, k * 16 * 128), idO, k > 0 ? 1u : acc0);
-            mma_commit(&ctl.ring_empty[slot]);
-            mma_commit(&ctl.pv_done[b]);
-          }
-          __syncwarp();
-          if (++slot == C::NST) {
-            slot = 0;
-            phase ^= 1;
+              for (int k = 0; k < C::BN / 16; ++k)
+                mma_bf16_ts(tO, tP + k * 8, sdesc_add(vdesc, k * 16 * 128), idO, k > 0 ? 1u : acc0);
+              mma_commit(&ctl.ring_empty[slot]);
+              if (u == C::VU - 1) mma_commit(&ctl.pv_done[b]);
+            }
+            __syncwarp();
           }
         }
       }
@@ -233,9 +232,7 @@ __global__ void __launch_bounds__(192, 1)
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
-      const int b = j & 1;
-      if (!(ok = mbar_wait(&ctl.s_full[b], (j >> 1) & 1, fs))) break;
-      tc_fence_after();
+      const uint32_t b = j & 1;
       int r, t;
       tile_of(it, j, r, t);
       const KeyRegion& kr = it.reg[r];
@@ -245,19 +242,18 @@ __global__ void __launch_bounds__(192, 1)
       const int hi = min(kr.count - 1, qpos - kr.pos0);
       const int clo = lo - kl0, chi = hi - kl0;  // allowed columns [clo, chi]
       const bool full = (clo <= 0) && (chi >= C::BN - 1);
+      if (!(ok = mbar_wait(&ctl.s_full[b], (j >> 1) & 1, fs))) break;
+      tc_fence_after();
 
       float s[C::BN];
 #pragma unroll
       for (int c4 = 0; c4 < C::BN / 32; ++c4) {
         uint32_t rr[32];
         tmem_ld32(tl + C::TM_S + b * C::BN + c4 * 32, rr);
-        tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[c4 * 32 + i] = __uint_as_float(rr[i]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.s_empty[b]);
+      tmem_ld_wait();
 
       float mx = -INFINITY;
       if (full) {
@@ -281,7 +277,7 @@ __global__ void __launch_bounds__(192, 1)
         if (!(ok = mbar_wait(&ctl.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, fs))) break;
         tc_fence_after();
 #pragma unroll
-        for (int c4 = 0; c4 < D / 32; ++c4) {
+        for (int c4 = 0; c4 < C::DV / 32; ++c4) {
           uint32_t rr[32];
           tmem_ld32(tl + C::TM_O + c4 * 32, rr);
           tmem_ld_wait();
@@ -294,27 +290,22 @@ __global__ void __launch_bounds__(192, 1)
         m = m_new;
       }
       const float m_use = (m == -INFINITY) ? 0.f : m;
-      // the P buffer is free once PV_{j-2} has completed
-      if (j >= 2 && !(ok = mbar_wait(&ctl.pv_done[b], ((j - 2) >> 1) & 1, fs))) break;
-      const uint32_t pb = smem_u32(sP + b * C::P_BYTES);
       float sum = 0.f;
 #pragma unroll
-      for (int ch = 0; ch < C::BN / 64; ++ch)
+      for (int h = 0; h < 2; ++h) {
+        uint32_t w[32];
 #pragma unroll
-        for (int pc = 0; pc < 8; ++pc) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = ch * 64 + pc * 8 + e * 2;
-            const float p0 = ex2_approx(fmaf(s[c], sl2, -m_use));
-            const float p1 = ex2_approx(fmaf(s[c + 1], sl2, -m_use));
-            sum += p0 + p1;
-            w[e] = pack_bf16x2(p0, p1);
-          }
-          st_shared_v4(pb + ch * C::BM * 128 + sw128_offset(row, pc), w[0], w[1], w[2], w[3]);
+        for (int e = 0; e < 32; ++e) {
+          const int c = h * 64 + 2 * e;
+          const float p0 = ex2_approx(fmaf(s[c], sl2, -m_use));
+          const float p1 = ex2_approx(fmaf(s[c + 1], sl2, -m_use));
+          sum += p0 + p1;
+          w[e] = pack_bf16x2(p0, p1);
         }
+        tmem_st32(tl + C::TM_S + b * C::BN + h * 32, w);
+      }
       l += sum;
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.p_full[b]);
@@ -326,9 +317,9 @@ __global__ void __launch_bounds__(192, 1)
       if (ok) {
         const bool valid = row < it.q_rows;
         const float inv_l = 1.f / l;
-        __nv_bfloat16* orow = a.out + ((int64_t)(it.q_row0 + row) * a.Hq + it.head) * D;
+        __nv_bfloat16* orow = a.out + ((int64_t)(it.q_row0 + row) * a.Hq + it.head) * D + split * C::DV;
 #pragma unroll
-        for (int c4 = 0; c4 < D / 32; ++c4) {
+        for (int c4 = 0; c4 < C::DV / 32; ++c4) {
           uint32_t rr[32];
           tmem_ld32(tl + C::TM_O + c4 * 32, rr);
           tmem_ld_wait();
@@ -342,7 +333,7 @@ __global__ void __launch_bounds__(192, 1)
             for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
           }
         }
-        if (valid) {
+        if (valid && split == 0) {
           const float m_use = (m == -INFINITY) ? 0.f : m;
           a.lse[(int64_t)it.head * a.T + it.q_row0 + row] = (m_use + __log2f(l)) * 0.69314718055994530942f;
         }
@@ -368,7 +359,7 @@ static cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, co
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  fwd_kernel<D><<<n_items, 192, C::SMEM_BYTES, st>>>(tq, tk, tv, a);
+  fwd_kernel<D><<<n_items * C::NSPLIT, 192, C::SMEM_BYTES, st>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
 
@@ -380,6 +371,8 @@ cudaError_t launch_fwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, cons
       return launch_fwd_d<64>(tq, tk, tv, a, n_items, st);
     case 128:
       return launch_fwd_d<128>(tq, tk, tv, a, n_items, st);
+    case 512:
+      return launch_fwd_d<512>(tq, tk, tv, a, n_items, st);
     default:
       return cudaErrorInvalidValue;
   }
