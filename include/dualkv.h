@@ -66,7 +66,7 @@ extern "C" {
  *   R_offsets      HOST int32[N+1], R_offsets[0] = 0, non-decreasing;
  *                  segment n has R_offsets[n+1] - R_offsets[n] >= 0 tokens
  *   Hq, Hkv        Hq % Hkv == 0
- *   D              head dimension: 64 or 128 (512: DUALKV_ERR_UNSUPPORTED in this build)
+ *   D              head dimension: 64, 128 or 512
  *   scale          softmax scale (typically 1/sqrt(D))
  *   window         <= 0: global causal; else sliding window of `window` keys
  *   out            device bf16 [T, Hq, D] (written)
@@ -78,7 +78,10 @@ int dualkv_fwd(const void* q, const void* k, const void* v, int P, int N, const 
 /*
  * Bytes of device workspace dualkv_bwd needs for this layout: the per-row
  * rowsum(dO * O) and log2-scaled LSE (2 * Hq * T fp32) plus the fp32 partial
- * dK/dV tiles of prompt key tiles whose query walk is split across CTAs.
+ * dK/dV tiles of prompt key tiles whose query walk is split across CTAs; for
+ * D = 512 also the bf16 P and dS blocks (2 x 32 KB per visited pair of a
+ * 128-row query tile and a 128-key tile), about 32 GB for P=16384, N=16,
+ * R=3072, Hq=8.
  * Returns 0 when the arguments are invalid.
  */
 size_t dualkv_bwd_workspace_bytes(int P, int N, const int32_t* R_offsets, int Hq, int Hkv, int D, int window);

@@ -45,7 +45,16 @@ struct DevPlan {
   ReduceItem* reduces = nullptr;
   int n_reduce = 0;
   int nslots = 0;
+  // head dimension 512
+  int32_t* block_base = nullptr;
+  int64_t n_blocks = 0;
+  XTItem* xt_items = nullptr;
+  int n_xt = 0;
+  XTEntry* xt_entries = nullptr;
   ~DevPlan() {
+    cudaFree(block_base);
+    cudaFree(xt_items);
+    cudaFree(xt_entries);
     cudaFree(fwd_items);
     cudaFree(dq_items);
     cudaFree(kv_items);
@@ -130,6 +139,21 @@ int get_plan(int P, int N, const int32_t* off, int Hq, int Hkv, int D, int windo
     pl->n_fwd = (int)items.size();
     pl->fwd_ready = true;
   }
+  if (need_bwd && !pl->bwd_ready && D == 512) {
+    auto dq = plan_qtiles(L, 128, 128);
+    if (upload(&pl->dq_items, dq) != cudaSuccess) return DUALKV_ERR_CUDA;
+    pl->n_dq = (int)dq.size();
+    Plan512 p5 = plan_512(L, dq, kMaxDkvIters);
+    if (upload(&pl->block_base, p5.block_base) != cudaSuccess) return DUALKV_ERR_CUDA;
+    if (upload(&pl->xt_items, p5.items) != cudaSuccess) return DUALKV_ERR_CUDA;
+    if (upload(&pl->xt_entries, p5.entries) != cudaSuccess) return DUALKV_ERR_CUDA;
+    if (upload(&pl->reduces, p5.reduces) != cudaSuccess) return DUALKV_ERR_CUDA;
+    pl->n_blocks = p5.n_blocks;
+    pl->n_xt = (int)p5.items.size();
+    pl->n_reduce = (int)p5.reduces.size();
+    pl->nslots = p5.nslots;
+    pl->bwd_ready = true;
+  }
   if (need_bwd && !pl->bwd_ready) {
     auto dq = plan_qtiles(L, dq_query_tile(D), dq_key_tile(D));
     if (upload(&pl->dq_items, dq) != cudaSuccess) return DUALKV_ERR_CUDA;
@@ -183,18 +207,34 @@ cudaError_t timed(int kind, cudaStream_t st, F&& launch) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct WsLayout {
-  size_t delta, lse2, partial, total;
+  size_t delta, lse2, partial, pblk, dsblk, total;
 };
-WsLayout ws_layout(int64_t T, int Hq, int D, int nslots) {
+// Delta | lse2 | fp32 split partials | (D = 512) P blocks | dS blocks
+WsLayout ws_layout(int64_t T, int Hq, int D, int nslots, int64_t n_blocks) {
   WsLayout w;
   w.delta = 0;
   w.lse2 = align256(sizeof(float) * (size_t)Hq * T);
   w.partial = w.lse2 + align256(sizeof(float) * (size_t)Hq * T);
-  w.total = w.partial + sizeof(float) * (size_t)nslots * 2 * dkv_key_tile(D) * D;
+  const int key_tile = D == 512 ? 128 : dkv_key_tile(D);
+  w.pblk = align256(w.partial + sizeof(float) * (size_t)nslots * 2 * key_tile * D);
+  w.dsblk = w.pblk + (size_t)n_blocks * 128 * 128 * 2;
+  w.total = w.dsblk + (size_t)n_blocks * 128 * 128 * 2;
   return w;
 }
 
-bool supported_d(int D) { return D == 64 || D == 128; }  // backward
+// [n_blocks, 128, 128] bf16 blocks, box 64 columns x box_rows rows x 1 block, 128-byte swizzle.
+int make_block_tmap(CUtensorMap* m, const void* base, int64_t n_blocks, int box_rows) {
+  cuuint64_t dims[3] = {128, 128, (cuuint64_t)n_blocks};
+  cuuint64_t strides[2] = {256, 128 * 256};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DUALKV_OK : DUALKV_ERR_CUDA;
+}
+
+bool supported_d(int D) { return D == 64 || D == 128 || D == 512; }  // backward
 bool supported_fwd_d(int D) { return D == 64 || D == 128 || D == 512; }
 
 }  // namespace
@@ -231,8 +271,12 @@ int dualkv_fwd(const void* q, const void* k, const void* v, int P, int N, const 
 size_t dualkv_bwd_workspace_bytes(int P, int N, const int32_t* R_offsets, int Hq, int Hkv, int D, int window) {
   if (validate_layout(P, N, R_offsets, Hq, Hkv, D) || !supported_d(D)) return 0;
   Layout L{P, N, std::vector<int32_t>(R_offsets, R_offsets + N + 1), Hq, Hkv, D, window <= 0 ? 0 : window};
+  if (D == 512) {
+    Plan512 p5 = plan_512(L, plan_qtiles(L, 128, 128), kMaxDkvIters);
+    return ws_layout(L.T(), Hq, D, p5.nslots, p5.n_blocks).total;
+  }
   KVPlan kv = plan_kvtiles(L, dkv_key_tile(D), dkv_query_block(D), kMaxDkvIters);
-  return ws_layout(L.T(), Hq, D, kv.nslots).total;
+  return ws_layout(L.T(), Hq, D, kv.nslots, 0).total;
 }
 
 int dualkv_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout, int P,
@@ -253,7 +297,7 @@ int dualkv_bwd(const void* q, const void* k, const void* v, const void* out, con
   if (rc) return rc;
   DevPlan* pl = nullptr;
   if ((rc = get_plan(P, N, R_offsets, Hq, Hkv, D, window, true, &pl))) return rc;
-  const WsLayout ws = ws_layout(T, Hq, D, pl->nslots);
+  const WsLayout ws = ws_layout(T, Hq, D, pl->nslots, D == 512 ? pl->n_blocks : 0);
   if (workspace_bytes < ws.total) return DUALKV_ERR_WORKSPACE;
   uint32_t* status = nullptr;
   if ((rc = status_word(pl->device, &status))) return rc;
@@ -266,6 +310,39 @@ int dualkv_bwd(const void* q, const void* k, const void* v, const void* out, con
 
   PrepArgs pa{static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, delta, lse2, T, Hq, D};
   if (timed(DUALKV_KERNEL_PREP, st, [&] { return launch_prep(pa, st); }) != cudaSuccess) return DUALKV_ERR_CUDA;
+
+  if (D == 512) {
+    __nv_bfloat16* pblk = reinterpret_cast<__nv_bfloat16*>(wsb + ws.pblk);
+    __nv_bfloat16* dsblk = reinterpret_cast<__nv_bfloat16*>(wsb + ws.dsblk);
+    CUtensorMap tq, tk, tv, tdo, tq64, tdo64, tk64, tP64, tDS64, tDS128;
+    if (make_tmap(&tq, q, T, Hq, D, 128) || make_tmap(&tk, k, T, Hkv, D, 128) || make_tmap(&tv, v, T, Hkv, D, 128) ||
+        make_tmap(&tdo, dout, T, Hq, D, 128) || make_tmap(&tq64, q, T, Hq, D, 64) ||
+        make_tmap(&tdo64, dout, T, Hq, D, 64) || make_tmap(&tk64, k, T, Hkv, D, 64) ||
+        make_block_tmap(&tP64, pblk, pl->n_blocks, 64) || make_block_tmap(&tDS64, dsblk, pl->n_blocks, 64) ||
+        make_block_tmap(&tDS128, dsblk, pl->n_blocks, 128))
+      return DUALKV_ERR_CUDA;
+    PdsArgs p0{pl->dq_items, pl->block_base, lse2, delta, nullptr, pblk, (int)T, Hq, Hkv, W, sl2, status};
+    PdsArgs p1{pl->dq_items, pl->block_base, lse2, delta, pblk, dsblk, (int)T, Hq, Hkv, W, sl2, status};
+    XtgArgs xv{pl->xt_items, pl->xt_entries, static_cast<__nv_bfloat16*>(dv), partial, 1, (int)T, Hq, Hkv, 1.f, status};
+    XtgArgs xk{pl->xt_items, pl->xt_entries, static_cast<__nv_bfloat16*>(dk), partial, 0, (int)T, Hq, Hkv, scale, status};
+    Dq512Args qa{pl->dq_items, pl->block_base, static_cast<__nv_bfloat16*>(dq), (int)T, Hq, Hkv, scale, status};
+    if (timed(DUALKV_KERNEL_DKV, st, [&] {
+          cudaError_t e = launch_pds(0, tq, tk, p0, pl->n_dq, st);
+          if (e == cudaSuccess) e = launch_pds(1, tdo, tv, p1, pl->n_dq, st);
+          if (e == cudaSuccess) e = launch_xtg(tP64, tdo64, xv, pl->n_xt, st);
+          if (e == cudaSuccess) e = launch_xtg(tDS64, tq64, xk, pl->n_xt, st);
+          return e;
+        }) != cudaSuccess)
+      return DUALKV_ERR_CUDA;
+    if (pl->n_reduce > 0) {
+      ReduceArgs ra{pl->reduces, partial, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), Hkv, D, 128};
+      if (timed(DUALKV_KERNEL_REDUCE, st, [&] { return launch_reduce(ra, pl->n_reduce, st); }) != cudaSuccess)
+        return DUALKV_ERR_CUDA;
+    }
+    if (timed(DUALKV_KERNEL_DQ, st, [&] { return launch_dq512(tDS128, tk64, qa, pl->n_dq, st); }) != cudaSuccess)
+      return DUALKV_ERR_CUDA;
+    return DUALKV_OK;
+  }
 
   CUtensorMap tq, tk, tv, tdo;
   if (make_tmap(&tq, q, T, Hq, D, dkv_query_block(D)) || make_tmap(&tk, k, T, Hkv, D, dkv_key_tile(D)) ||

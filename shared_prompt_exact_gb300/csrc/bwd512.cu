@@ -1,0 +1,566 @@
+// bwd512.cu -- DualKV backward for head dimension 512 (sm_103a).
+//
+// With D = 512 a 128-row tile of Q or dO is 128 KB and a 128 x 512 fp32
+// accumulator fills all 512 TMEM columns, so the fused dQ and dK/dV kernels
+// of bwd.cu do not fit.  This backward materialises the two 128 x 128 bf16
+// blocks of every (query tile, key tile) pair the walk visits, then reduces
+// them with plain tensor-core GEMMs -- no product is computed twice:
+//   pds<0>:  S = Q K^T  ->  P  = exp(S - LSE)           (masked, bf16 block)
+//   pds<1>:  dP = dO V^T -> dS = P (dP - Delta)         (bf16 block)
+//   xtg:     dV = sum P^T dO,  dK = scale sum dS^T Q    (per key tile; fixed order)
+//   dq512:   dQ = scale sum dS K                        (per query tile)
+// The formulas are the analytic backward of softmax attention; the fold of
+// the replicated prompt gradients is the sum over all query tiles (of every
+// segment) that attend a prompt key tile, in the fixed order of the plan.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dkv {
+
+namespace {
+
+constexpr int kD = 512;
+constexpr int kBlkBytes = 128 * 128 * 2;  // one P or dS block
+
+__device__ __forceinline__ void walk_tile(const QTileItem& it, int j, int& r, int& t) {
+  const int n0 = it.reg[0].t_hi - it.reg[0].t_lo;
+  if (j < n0) {
+    r = 0;
+    t = it.reg[0].t_lo + j;
+  } else {
+    r = 1;
+    t = it.reg[1].t_lo + (j - n0);
+  }
+}
+
+// ---------------------------------------------------------------- P / dS blocks
+struct PdsCfg {
+  static constexpr int BM = 128, BN = 128;
+  static constexpr int QCH = kD / 64;          // chunks of the resident operand
+  static constexpr int UNIT_BYTES = 2 * BN * 128;  // two 64-column chunks of a key tile
+  static constexpr int KU = QCH / 2;           // units per key tile
+  static constexpr int A_BYTES = BM * kD * 2;  // 128 KB
+  static constexpr int NST = 3;
+  static constexpr int SMEM_BYTES = A_BYTES + NST * UNIT_BYTES + 1024;
+  static constexpr uint32_t TM_COLS = 256;     // two S buffers
+};
+
+struct PdsCtl {
+  uint64_t a_full;
+  uint64_t ring_full[3], ring_empty[3];
+  uint64_t s_full[2], s_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// MODE 0: A = Q, B = K, writes P blocks.  MODE 1: A = dO, B = V, reads P, writes dS blocks.
+template <int MODE>
+__global__ void __launch_bounds__(192, 1)
+    pds_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const PdsArgs a) {
+  using C = PdsCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ PdsCtl ctl;
+  uint8_t* sA = smem;
+  uint8_t* sRing = smem + C::A_BYTES;
+
+  const QTileItem it = a.items[blockIdx.x];
+  const int blk0 = a.block_base[blockIdx.x];
+  const int nt = (it.reg[0].t_hi - it.reg[0].t_lo) + (it.reg[1].t_hi - it.reg[1].t_lo);
+  const int kvh = it.head / (a.Hq / a.Hkv);
+  const uint32_t warp = warp_id(), lane = lane_id();
+  FailState fs{&ctl.abort_flag, a.status};
+
+  if (threadIdx.x == 0) {
+    ctl.abort_flag = 0;
+    mbar_init(&ctl.a_full, 1);
+    for (int i = 0; i < C::NST; ++i) {
+      mbar_init(&ctl.ring_full[i], 1);
+      mbar_init(&ctl.ring_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl.s_full[i], 1);
+      mbar_init(&ctl.s_empty[i], 4);
+    }
+    mbar_init(&ctl.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl.tmem_base, C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0 && nt > 0) {
+      mbar_arrive_expect_tx(&ctl.a_full, C::A_BYTES);
+      for (int c = 0; c < C::QCH; ++c) tma_load_3d(sA + c * C::BM * 128, &tmA, &ctl.a_full, c * 64, it.head, it.q_row0);
+      int idx = 0;
+      bool ok = true;
+      for (int j = 0; j < nt && ok; ++j) {
+        int r, t;
+        walk_tile(it, j, r, t);
+        const int key_row = it.reg[r].row0 + t * C::BN;
+        for (int u = 0; u < C::KU; ++u, ++idx) {
+          const int slot = idx % C::NST;
+          if (!(ok = mbar_wait(&ctl.ring_empty[slot], ((idx / C::NST) & 1) ^ 1, fs))) break;
+          mbar_arrive_expect_tx(&ctl.ring_full[slot], C::UNIT_BYTES);
+          uint8_t* dst = sRing + slot * C::UNIT_BYTES;
+          for (int c = 0; c < 2; ++c)
+            tma_load_3d(dst + c * C::BN * 128, &tmB, &ctl.ring_full[slot], (2 * u + c) * 64, kvh, key_row);
+        }
+      }
+      if (!ok) {
+        mbar_wait_drain(&ctl.a_full, 0, kWaitLimitNs);
+        for (int back = 1; back <= C::NST && back <= idx; ++back) {
+          const int i2 = idx - back;
+          mbar_wait_drain(&ctl.ring_full[i2 % C::NST], (i2 / C::NST) & 1, kWaitLimitNs);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (nt > 0) {
+      constexpr uint32_t idS = idesc_bf16(128, C::BN, 0, 0);
+      const uint64_t adesc = sdesc_sw128(smem_u32(sA), 16, 1024);
+      const uint32_t aRing = smem_u32(sRing);
+      bool ok = mbar_wait(&ctl.a_full, 0, fs);
+      tc_fence_after();
+      int idx = 0;
+      for (int j = 0; j < nt && ok; ++j) {
+        const uint32_t b = j & 1;
+        if (!(ok = mbar_wait(&ctl.s_empty[b], ((j >> 1) & 1) ^ 1, fs))) break;
+        const uint32_t tS = tmem + b * C::BN;
+        for (int u = 0; u < C::KU && ok; ++u, ++idx) {
+          const int slot = idx % C::NST;
+          if (!(ok = mbar_wait(&ctl.ring_full[slot], (idx / C::NST) & 1, fs))) break;
+          tc_fence_after();
+          const uint64_t bdesc = sdesc_sw128(aRing + slot * C::UNIT_BYTES, 16, 1024);
+          const uint64_t ad = sdesc_add(adesc, u * 2 * C::BM * 128);
+          if (elect_one()) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_bf16_ss(tS, sdesc_add(ad, c * C::BM * 128 + k * 32), sdesc_add(bdesc, c * C::BN * 128 + k * 32),
+                            idS, (u | c | k) != 0);
+            mma_commit(&ctl.ring_empty[slot]);
+            if (u == C::KU - 1) mma_commit(&ctl.s_full[b]);
+          }
+          __syncwarp();
+        }
+      }
+      if (elect_one()) mma_commit(&ctl.drain);
+      __syncwarp();
+      mbar_wait_drain(&ctl.drain, 0, kWaitLimitNs);
+    }
+  } else {
+    // thread <-> query row; each tile yields one 256-byte row of the output block
+    const uint32_t wq = warp & 3;
+    const int row = (int)(wq * 32 + lane);
+    const uint32_t tl = tmem + ((wq * 32) << 16);
+    const int qpos = it.q_pos0 + row;
+    const bool valid = row < it.q_rows;
+    const int64_t rix = (int64_t)it.head * a.T + it.q_row0 + row;
+    const float lse2 = (MODE == 0 && valid) ? a.lse2[rix] : INFINITY;
+    const float delta = (MODE == 1 && valid) ? a.delta[rix] : 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      const uint32_t b = j & 1;
+      if (!(ok = mbar_wait(&ctl.s_full[b], (j >> 1) & 1, fs))) break;
+      tc_fence_after();
+      float s[C::BN];
+#pragma unroll
+      for (int c4 = 0; c4 < C::BN / 32; ++c4) {
+        uint32_t rr[32];
+        tmem_ld32(tl + b * C::BN + c4 * 32, rr);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c4 * 32 + i] = __uint_as_float(rr[i]);
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.s_empty[b]);
+      const size_t boff = (size_t)(blk0 + j) * (kBlkBytes / 2) + (size_t)row * C::BN;
+      uint4* dst = reinterpret_cast<uint4*>(a.out_blocks + boff);
+      if (MODE == 0) {
+        int r, t;
+        walk_tile(it, j, r, t);
+        const KeyRegion& kr = it.reg[r];
+        const int kl0 = t * C::BN;
+        int lo = 0;
+        if (a.window > 0) lo = max(0, qpos - a.window + 1 - kr.pos0);
+        const int hi = min(kr.count - 1, qpos - kr.pos0);
+        const int clo = lo - kl0, chi = hi - kl0;
+#pragma unroll
+        for (int v = 0; v < C::BN / 8; ++v) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 8 * v + 2 * e;
+            float p0 = ex2_approx(fmaf(s[c], a.scale_log2, -lse2));
+            float p1 = ex2_approx(fmaf(s[c + 1], a.scale_log2, -lse2));
+            p0 = (c < clo || c > chi) ? 0.f : p0;
+            p1 = (c + 1 < clo || c + 1 > chi) ? 0.f : p1;
+            w[e] = pack_bf16x2(p0, p1);
+          }
+          dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else {
+        const uint4* src = reinterpret_cast<const uint4*>(a.p_blocks + boff);
+#pragma unroll
+        for (int v = 0; v < C::BN / 8; ++v) {
+          const uint4 pin = src[v];
+          const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&pin);
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 8 * v + 2 * e;
+            const float2 p = __bfloat1622float2(p2[e]);
+            w[e] = pack_bf16x2(p.x * (s[c] - delta), p.y * (s[c + 1] - delta));
+          }
+          dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
+}
+
+// ---------------------------------------------------------------- transposed GEMMs (dV, dK)
+// out[key, :] = mul * sum over the entries e of the key tile: A_e^T B_e, with
+// A_e the 64 query rows x 128 keys of a P (or dS) block and B_e the same 64
+// query rows of dO (or Q), all 512 columns.  Both operands are MN-major.
+struct XtgCfg {
+  static constexpr int A_BYTES = 2 * 64 * 128;       // 2 key chunks x 64 query rows
+  static constexpr int B_BYTES = 8 * 64 * 128;       // 8 column chunks x 64 query rows
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int NST = 2;
+  static constexpr int SMEM_BYTES = NST * STAGE_BYTES + 1024;
+  static constexpr uint32_t TM_COLS = 512;
+};
+
+struct XtgCtl {
+  uint64_t full[2], empty[2];
+  uint64_t acc_done, drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__global__ void __launch_bounds__(192, 1)
+    xtg_kernel(const __grid_constant__ CUtensorMap tmBlk, const __grid_constant__ CUtensorMap tmB, const XtgArgs a) {
+  using C = XtgCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ XtgCtl ctl;
+  const XTItem it = a.items[blockIdx.x];
+  const int n_iter = it.it_hi - it.it_lo;
+  const uint32_t warp = warp_id(), lane = lane_id();
+  FailState fs{&ctl.abort_flag, a.status};
+
+  if (threadIdx.x == 0) {
+    ctl.abort_flag = 0;
+    for (int i = 0; i < C::NST; ++i) {
+      mbar_init(&ctl.full[i], 1);
+      mbar_init(&ctl.empty[i], 1);
+    }
+    mbar_init(&ctl.acc_done, 1);
+    mbar_init(&ctl.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl.tmem_base, C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0 && n_iter > 0) {
+      bool ok = true;
+      int i = 0;
+      for (; i < n_iter; ++i) {
+        const XTEntry e = a.entries[it.list_begin + it.it_lo + i];
+        const int slot = i % C::NST;
+        if (!(ok = mbar_wait(&ctl.empty[slot], ((i / C::NST) & 1) ^ 1, fs))) break;
+        mbar_arrive_expect_tx(&ctl.full[slot], C::STAGE_BYTES);
+        uint8_t* st = smem + slot * C::STAGE_BYTES;
+        for (int kc = 0; kc < 2; ++kc)
+          tma_load_3d(st + kc * 64 * 128, &tmBlk, &ctl.full[slot], kc * 64, e.sub * 64, e.block);
+        for (int c = 0; c < 8; ++c)
+          tma_load_3d(st + C::A_BYTES + c * 64 * 128, &tmB, &ctl.full[slot], c * 64, e.head, e.q_row0);
+      }
+      if (!ok) {
+        for (int back = 1; back <= C::NST && back <= i; ++back) {
+          const int i2 = i - back;
+          mbar_wait_drain(&ctl.full[i2 % C::NST], (i2 / C::NST) & 1, kWaitLimitNs);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (n_iter > 0) {
+      constexpr uint32_t idX = idesc_bf16(128, 256, 1, 1);
+      const uint32_t base = smem_u32(smem);
+      bool ok = true;
+      for (int i = 0; i < n_iter && ok; ++i) {
+        const int slot = i % C::NST;
+        if (!(ok = mbar_wait(&ctl.full[slot], (i / C::NST) & 1, fs))) break;
+        tc_fence_after();
+        const uint64_t ad = sdesc_sw128(base + slot * C::STAGE_BYTES, 64 * 128, 1024);
+        const uint64_t bd = sdesc_sw128(base + slot * C::STAGE_BYTES + C::A_BYTES, 64 * 128, 1024);
+        const uint32_t acc0 = i > 0 ? 1u : 0u;
+        if (elect_one()) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int nh = 0; nh < 2; ++nh)
+              mma_bf16_ss(tmem + nh * 256, sdesc_add(ad, k * 16 * 128), sdesc_add(bd, nh * 4 * 64 * 128 + k * 16 * 128),
+                          idX, k > 0 ? 1u : acc0);
+          mma_commit(&ctl.empty[slot]);
+        }
+        __syncwarp();
+      }
+      if (elect_one()) {
+        if (ok) mma_commit(&ctl.acc_done);
+        mma_commit(&ctl.drain);
+      }
+      __syncwarp();
+      mbar_wait_drain(&ctl.drain, 0, kWaitLimitNs);
+    }
+  } else {
+    // epilogue: thread <-> key row
+    const uint32_t wq = warp & 3;
+    const int row = (int)(wq * 32 + lane);
+    const uint32_t tl = tmem + ((wq * 32) << 16);
+    const bool kvalid = row < it.k_rows;
+    bool ok = true;
+    if (n_iter > 0) {
+      ok = mbar_wait(&ctl.acc_done, 0, fs);
+      tc_fence_after();
+    }
+    if (ok) {
+      float* pdst = it.partial_slot >= 0
+                        ? a.partial + (((size_t)it.partial_slot * 2 + a.region) * 128 + row) * kD
+                        : nullptr;
+      __nv_bfloat16* odst = a.out + ((int64_t)(it.k_row0 + row) * a.Hkv + it.kv_head) * kD;
+#pragma unroll 1
+      for (int c4 = 0; c4 < kD / 32; ++c4) {
+        uint32_t rr[32];
+        if (n_iter > 0) {
+          tmem_ld32(tl + c4 * 32, rr);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) rr[e] = 0u;
+        }
+        if (!kvalid) continue;
+        if (pdst) {
+          float4* d4 = reinterpret_cast<float4*>(pdst + c4 * 32);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            d4[v] = make_float4(__uint_as_float(rr[4 * v]) * a.mul, __uint_as_float(rr[4 * v + 1]) * a.mul,
+                                __uint_as_float(rr[4 * v + 2]) * a.mul, __uint_as_float(rr[4 * v + 3]) * a.mul);
+        } else {
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(rr[2 * e]) * a.mul, __uint_as_float(rr[2 * e + 1]) * a.mul);
+          uint4* d = reinterpret_cast<uint4*>(odst + c4 * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) d[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
+}
+
+// ---------------------------------------------------------------- dQ GEMM
+// dQ[q tile, :] = scale * sum over the tile's key walk of dS_blk K, one 64-key
+// half of a block per step: A = dS (128 q x 64 keys, K-major), B = 64 key rows
+// of K, all 512 columns (MN-major).
+struct Dq512Cfg {
+  static constexpr int A_BYTES = 128 * 128;   // 128 rows x 64 keys
+  static constexpr int B_BYTES = 8 * 64 * 128;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int NST = 2;
+  static constexpr int SMEM_BYTES = NST * STAGE_BYTES + 1024;
+  static constexpr uint32_t TM_COLS = 512;
+};
+
+__global__ void __launch_bounds__(192, 1)
+    dq512_kernel(const __grid_constant__ CUtensorMap tmBlk, const __grid_constant__ CUtensorMap tmK, const Dq512Args a) {
+  using C = Dq512Cfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ XtgCtl ctl;
+  const QTileItem it = a.items[blockIdx.x];
+  const int blk0 = a.block_base[blockIdx.x];
+  const int nt = (it.reg[0].t_hi - it.reg[0].t_lo) + (it.reg[1].t_hi - it.reg[1].t_lo);
+  const int n_iter = 2 * nt;
+  const int kvh = it.head / (a.Hq / a.Hkv);
+  const uint32_t warp = warp_id(), lane = lane_id();
+  FailState fs{&ctl.abort_flag, a.status};
+
+  if (threadIdx.x == 0) {
+    ctl.abort_flag = 0;
+    for (int i = 0; i < C::NST; ++i) {
+      mbar_init(&ctl.full[i], 1);
+      mbar_init(&ctl.empty[i], 1);
+    }
+    mbar_init(&ctl.acc_done, 1);
+    mbar_init(&ctl.drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl.tmem_base, C::TM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl.tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0 && n_iter > 0) {
+      bool ok = true;
+      int i = 0;
+      for (; i < n_iter; ++i) {
+        const int j = i >> 1, half = i & 1;
+        int r, t;
+        walk_tile(it, j, r, t);
+        const int key_row = it.reg[r].row0 + t * 128 + half * 64;
+        const int slot = i % C::NST;
+        if (!(ok = mbar_wait(&ctl.empty[slot], ((i / C::NST) & 1) ^ 1, fs))) break;
+        mbar_arrive_expect_tx(&ctl.full[slot], C::STAGE_BYTES);
+        uint8_t* st = smem + slot * C::STAGE_BYTES;
+        tma_load_3d(st, &tmBlk, &ctl.full[slot], half * 64, 0, blk0 + j);
+        for (int c = 0; c < 8; ++c) tma_load_3d(st + C::A_BYTES + c * 64 * 128, &tmK, &ctl.full[slot], c * 64, kvh, key_row);
+      }
+      if (!ok) {
+        for (int back = 1; back <= C::NST && back <= i; ++back) {
+          const int i2 = i - back;
+          mbar_wait_drain(&ctl.full[i2 % C::NST], (i2 / C::NST) & 1, kWaitLimitNs);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (n_iter > 0) {
+      constexpr uint32_t idQ = idesc_bf16(128, 256, 0, 1);
+      const uint32_t base = smem_u32(smem);
+      bool ok = true;
+      for (int i = 0; i < n_iter && ok; ++i) {
+        const int slot = i % C::NST;
+        if (!(ok = mbar_wait(&ctl.full[slot], (i / C::NST) & 1, fs))) break;
+        tc_fence_after();
+        const uint64_t ad = sdesc_sw128(base + slot * C::STAGE_BYTES, 16, 1024);
+        const uint64_t bd = sdesc_sw128(base + slot * C::STAGE_BYTES + C::A_BYTES, 64 * 128, 1024);
+        const uint32_t acc0 = i > 0 ? 1u : 0u;
+        if (elect_one()) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int nh = 0; nh < 2; ++nh)
+              mma_bf16_ss(tmem + nh * 256, sdesc_add(ad, k * 32), sdesc_add(bd, nh * 4 * 64 * 128 + k * 16 * 128), idQ,
+                          k > 0 ? 1u : acc0);
+          mma_commit(&ctl.empty[slot]);
+        }
+        __syncwarp();
+      }
+      if (elect_one()) {
+        if (ok) mma_commit(&ctl.acc_done);
+        mma_commit(&ctl.drain);
+      }
+      __syncwarp();
+      mbar_wait_drain(&ctl.drain, 0, kWaitLimitNs);
+    }
+  } else {
+    const uint32_t wq = warp & 3;
+    const int row = (int)(wq * 32 + lane);
+    const uint32_t tl = tmem + ((wq * 32) << 16);
+    const bool valid = row < it.q_rows;
+    bool ok = n_iter > 0 && mbar_wait(&ctl.acc_done, 0, fs);
+    tc_fence_after();
+    if (ok) {
+      __nv_bfloat16* qrow = a.dq + ((int64_t)(it.q_row0 + row) * a.Hq + it.head) * kD;
+#pragma unroll 1
+      for (int c4 = 0; c4 < kD / 32; ++c4) {
+        uint32_t rr[32];
+        tmem_ld32(tl + c4 * 32, rr);
+        tmem_ld_wait();
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          w[e] = pack_bf16x2(__uint_as_float(rr[2 * e]) * a.scale, __uint_as_float(rr[2 * e + 1]) * a.scale);
+        if (valid) {
+          uint4* d = reinterpret_cast<uint4*>(qrow + c4 * 32);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) d[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, int bytes, bool& done) {
+  if (done) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done = true;
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_pds(int mode, const CUtensorMap& tA, const CUtensorMap& tB, const PdsArgs& a, int n_items,
+                       cudaStream_t st) {
+  if (n_items <= 0) return cudaSuccess;
+  static bool s0 = false, s1 = false;
+  cudaError_t e;
+  if (mode == 0) {
+    if ((e = set_smem(pds_kernel<0>, PdsCfg::SMEM_BYTES, s0)) != cudaSuccess) return e;
+    pds_kernel<0><<<n_items, 192, PdsCfg::SMEM_BYTES, st>>>(tA, tB, a);
+  } else {
+    if ((e = set_smem(pds_kernel<1>, PdsCfg::SMEM_BYTES, s1)) != cudaSuccess) return e;
+    pds_kernel<1><<<n_items, 192, PdsCfg::SMEM_BYTES, st>>>(tA, tB, a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_xtg(const CUtensorMap& tBlk, const CUtensorMap& tB, const XtgArgs& a, int n_items, cudaStream_t st) {
+  if (n_items <= 0) return cudaSuccess;
+  static bool s = false;
+  cudaError_t e = set_smem(xtg_kernel, XtgCfg::SMEM_BYTES, s);
+  if (e != cudaSuccess) return e;
+  xtg_kernel<<<n_items, 192, XtgCfg::SMEM_BYTES, st>>>(tBlk, tB, a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq512(const CUtensorMap& tBlk, const CUtensorMap& tK, const Dq512Args& a, int n_items,
+                         cudaStream_t st) {
+  if (n_items <= 0) return cudaSuccess;
+  static bool s = false;
+  cudaError_t e = set_smem(dq512_kernel, Dq512Cfg::SMEM_BYTES, s);
+  if (e != cudaSuccess) return e;
+  dq512_kernel<<<n_items, 192, Dq512Cfg::SMEM_BYTES, st>>>(tBlk, tK, a);
+  return cudaGetLastError();
+}
+
+}  // namespace dkv

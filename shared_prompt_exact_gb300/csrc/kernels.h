@@ -77,6 +77,44 @@ struct ReduceArgs {
 };
 cudaError_t launch_reduce(const ReduceArgs& a, int n_items, cudaStream_t st);
 
+// ---- head dimension 512 backward (bwd512.cu)
+struct PdsArgs {
+  const QTileItem* items;
+  const int32_t* block_base;
+  const float* lse2;
+  const float* delta;
+  const __nv_bfloat16* p_blocks;  // mode 1 input
+  __nv_bfloat16* out_blocks;      // mode 0: P blocks, mode 1: dS blocks
+  int T, Hq, Hkv, window;
+  float scale_log2;
+  uint32_t* status;
+};
+cudaError_t launch_pds(int mode, const CUtensorMap& tA, const CUtensorMap& tB, const PdsArgs& a, int n_items,
+                       cudaStream_t st);
+
+struct XtgArgs {
+  const XTItem* items;
+  const XTEntry* entries;
+  __nv_bfloat16* out;  // dV or dK [T, Hkv, 512]
+  float* partial;      // [slot][2][128][512]
+  int region;          // partial half: 0 = dK, 1 = dV
+  int T, Hq, Hkv;
+  float mul;
+  uint32_t* status;
+};
+cudaError_t launch_xtg(const CUtensorMap& tBlk, const CUtensorMap& tB, const XtgArgs& a, int n_items, cudaStream_t st);
+
+struct Dq512Args {
+  const QTileItem* items;
+  const int32_t* block_base;
+  __nv_bfloat16* dq;
+  int T, Hq, Hkv;
+  float scale;
+  uint32_t* status;
+};
+cudaError_t launch_dq512(const CUtensorMap& tBlk, const CUtensorMap& tK, const Dq512Args& a, int n_items,
+                         cudaStream_t st);
+
 // One CTA waits on an mbarrier that nothing completes, with a bounded wait of limit_ns.
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, uint32_t* status, cudaStream_t st);
 

@@ -160,4 +160,86 @@ KVPlan plan_kvtiles(const Layout& L, int key_tile, int q_block, int max_iters) {
   return plan;
 }
 
+Plan512 plan_512(const Layout& L, const std::vector<QTileItem>& qitems, int max_iters) {
+  Plan512 pl;
+  const int gs = L.Hq / L.Hkv;
+  constexpr int kTile = 128;
+  // key tiles: prompt tiles first, then each segment's tiles
+  std::vector<int32_t> seg_tile_base(L.N + 1, 0);
+  const int prompt_tiles = (L.P + kTile - 1) / kTile;
+  int ntiles = prompt_tiles;
+  for (int n = 0; n < L.N; ++n) {
+    seg_tile_base[n] = ntiles;
+    ntiles += (L.off[n + 1] - L.off[n] + kTile - 1) / kTile;
+  }
+  pl.block_base.resize(qitems.size());
+  int64_t nb = 0;
+  for (size_t i = 0; i < qitems.size(); ++i) {
+    pl.block_base[i] = (int32_t)nb;
+    nb += (qitems[i].reg[0].t_hi - qitems[i].reg[0].t_lo) + (qitems[i].reg[1].t_hi - qitems[i].reg[1].t_lo);
+  }
+  pl.n_blocks = nb;
+  // the segment whose rows begin at `row0` (and hold at least one row)
+  auto seg_of_row = [&](int32_t row0) {
+    for (int n = 0; n < L.N; ++n)
+      if (L.P + L.off[n] == row0 && L.off[n + 1] > L.off[n]) return n;
+    return -1;
+  };
+  // walk the query tiles in fixed order: group heads ascending, then packed row order
+  std::vector<size_t> order(qitems.size());
+  for (size_t i = 0; i < order.size(); ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](size_t a, size_t b) {
+    if (qitems[a].head != qitems[b].head) return qitems[a].head < qitems[b].head;
+    return qitems[a].q_row0 < qitems[b].q_row0;
+  });
+  std::vector<std::vector<XTEntry>> lists((size_t)ntiles * L.Hkv);
+  for (size_t oi : order) {
+    const QTileItem& it = qitems[oi];
+    const int g = it.head / gs;
+    int j = 0;
+    for (int r = 0; r < 2; ++r) {
+      const KeyRegion& kr = it.reg[r];
+      const int base = r == 0 ? 0 : (kr.t_hi > kr.t_lo ? seg_tile_base[seg_of_row(kr.row0)] : 0);
+      for (int t = kr.t_lo; t < kr.t_hi; ++t, ++j) {
+        auto& lst = lists[(size_t)(base + t) * L.Hkv + g];
+        for (int sub = 0; sub < 2; ++sub)
+          if (sub * 64 < it.q_rows) lst.push_back(XTEntry{it.head, it.q_row0 + sub * 64, pl.block_base[oi] + j, sub});
+      }
+    }
+  }
+  // key tile geometry in the same numbering
+  std::vector<std::pair<int32_t, int32_t>> ktile(ntiles);  // (row0, rows)
+  for (int t = 0; t < prompt_tiles; ++t) ktile[t] = {t * kTile, std::min(kTile, L.P - t * kTile)};
+  for (int n = 0; n < L.N; ++n) {
+    const int R = L.off[n + 1] - L.off[n];
+    for (int t = 0; t * kTile < R; ++t) ktile[seg_tile_base[n] + t] = {L.P + L.off[n] + t * kTile, std::min(kTile, R - t * kTile)};
+  }
+  for (int g = 0; g < L.Hkv; ++g)
+    for (int kt = 0; kt < ntiles; ++kt) {
+      const auto& lst = lists[(size_t)kt * L.Hkv + g];
+      const int begin = (int)pl.entries.size();
+      pl.entries.insert(pl.entries.end(), lst.begin(), lst.end());
+      const int total = (int)lst.size();
+      const int nsplit = std::max(1, (total + max_iters - 1) / max_iters);
+      const int chunk = std::max(1, (total + nsplit - 1) / nsplit);
+      const int slot0 = pl.nslots;
+      int made = 0;
+      for (int lo = 0; lo < std::max(total, 1); lo += chunk, ++made) {
+        XTItem x{};
+        x.k_row0 = ktile[kt].first;
+        x.k_rows = ktile[kt].second;
+        x.kv_head = g;
+        x.list_begin = begin;
+        x.it_lo = lo;
+        x.it_hi = std::min(total, lo + chunk);
+        x.partial_slot = nsplit > 1 ? pl.nslots++ : -1;
+        pl.items.push_back(x);
+      }
+      if (nsplit > 1) pl.reduces.push_back(ReduceItem{ktile[kt].first, ktile[kt].second, g, slot0, made, 0});
+    }
+  std::stable_sort(pl.items.begin(), pl.items.end(),
+                   [](const XTItem& a, const XTItem& b) { return (a.it_hi - a.it_lo) > (b.it_hi - b.it_lo); });
+  return pl;
+}
+
 }  // namespace dkv

@@ -75,6 +75,35 @@ struct KVPlan {
 // whose walk exceeds `max_iters` iterations is split into contiguous chunks.
 KVPlan plan_kvtiles(const Layout& L, int key_tile, int q_block, int max_iters);
 
+// ---------------------------------------------------------------------------
+// Head dimension 512 backward.  The 128 x 512 operand and accumulator tiles do
+// not fit the fused dQ and dK/dV kernels, so the backward materialises the
+// attention probabilities P and dS = P (dP - Delta) as bf16 blocks of 128 query
+// rows x 128 keys in device memory, then reduces them with plain GEMMs.
+// Block ids: query-tile item i (in the given list) owns blocks
+// block_base[i] .. block_base[i] + (its key tiles) - 1, in walk order.
+//
+// One step of the dK / dV GEMM: the 64 query rows `sub` (0 or 1) of block
+// `block`, i.e. rows q_row0 .. q_row0 + 63 of q-head `head`.
+struct XTEntry {
+  int32_t head, q_row0, block, sub;
+};
+// dK/dV GEMM work item: key tile x kv-head x chunk [it_lo, it_hi) of its
+// entry list (group heads ascending, then query tiles in packed order).
+struct XTItem {
+  int32_t k_row0, k_rows, kv_head, list_begin, it_lo, it_hi, partial_slot, pad_;
+};
+struct Plan512 {
+  std::vector<int32_t> block_base;  // per query-tile item
+  int64_t n_blocks = 0;
+  std::vector<XTItem> items;        // heaviest first
+  std::vector<XTEntry> entries;
+  std::vector<ReduceItem> reduces;
+  int nslots = 0;
+};
+// `qitems` must come from plan_qtiles(L, 128, 128).
+Plan512 plan_512(const Layout& L, const std::vector<QTileItem>& qitems, int max_iters);
+
 // Host index builder (see dualkv_build_index).
 void build_index(int P, int N, const int32_t* off, int32_t* seg_id, int32_t* pos_id, int32_t* cu_rep,
                  int32_t* rep2pack);
