@@ -88,28 +88,39 @@ __device__ __forceinline__ uint32_t packed_kstep_col(int k) { return 32u * (k >>
 __device__ __forceinline__ uint32_t packed_kstep_col64(int k) { return 64u * (k >> 2) + 8u * (k & 3); }
 
 // ---------------------------------------------------------------- dQ
-// 128-key tiles: S and dP are M=128 x N=128 MMAs.  S is double-buffered (its
-// buffer also carries dS to the dQ GEMM); dP is single-buffered and released
-// as soon as the compute warps have loaded it.  Each compute thread handles 64
-// key columns of its query row.  TMEM: S 2 x 128, dP 128, dQ D columns.
+// 128-key tiles: S and dP are M=128 x N=128 MMAs.  S and dP each have one TMEM
+// buffer, released as soon as the compute warps have loaded them, so the next
+// tile's S and dP run while the compute warps work.  dS goes to its own
+// double buffer (nothing the tensor pipe writes aliases what it reads).  NG
+// compute warps share each TMEM lane quarter; each thread handles BN / NG key
+// columns of its query row (two warps per quarter measured fastest: four were
+// slower).
+// TMEM: S 128 | dP 128 | dS 2 x 64 | dQ D columns.
 template <int D>
 struct DqCfg {
   static constexpr int BM = 128, BN = 128;
+  static constexpr int NG = 2;                       // compute warps per TMEM lane quarter
+  static constexpr int GC = BN / NG;                 // key columns of one compute warp
+  static constexpr int THREADS = 64 + 128 * NG;
   static constexpr int KCH = D / 64;
   static constexpr int Q_BYTES = BM * D * 2;         // Q and dO tiles (resident)
   static constexpr int TILE_BYTES = BN * D * 2;      // one K or V tile
-  static constexpr int NST = (D == 128) ? 5 : 10;
+  // K tiles stay until their dQ GEMM (a step later), V tiles only until dP:
+  // separate rings keep a slow-to-free K slot from holding up the next V load
+  static constexpr int NSK = (D == 128) ? 3 : 6;
+  static constexpr int NSV = (D == 128) ? 2 : 6;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = OFF_Q + Q_BYTES;
-  static constexpr int OFF_RING = OFF_DO + Q_BYTES;
-  static constexpr int SMEM_BYTES = OFF_RING + NST * TILE_BYTES + 1024;
-  static constexpr uint32_t TM_S = 0, TM_DP = 2 * BN, TM_DQ = 3 * BN, TM_COLS = 512;
+  static constexpr int OFF_KR = OFF_DO + Q_BYTES;
+  static constexpr int OFF_VR = OFF_KR + NSK * TILE_BYTES;
+  static constexpr int SMEM_BYTES = OFF_VR + NSV * TILE_BYTES + 1024;
+  static constexpr uint32_t TM_S = 0, TM_DP = BN, TM_DS = 2 * BN, TM_DQ = 3 * BN, TM_COLS = 512;
 };
 
 struct DqSmemCtl {
   uint64_t q_full;
-  uint64_t ring_full[10], ring_empty[10];
-  uint64_t s_full[2], ds_full[2], dp_empty;
+  uint64_t k_full[6], k_empty[6], v_full[6], v_empty[6];
+  uint64_t s_full, s_empty, dp_empty, ds_full[2], ds_done[2];
   uint64_t acc_done, drain;
   uint32_t tmem_base;
   int abort_flag;
@@ -127,7 +138,7 @@ __device__ __forceinline__ void qtile_of(const QTileItem& it, int j, int& r, int
 }
 
 template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const DqArgs a) {
   using C = DqCfg<D>;
@@ -136,7 +147,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __shared__ DqSmemCtl ctl;
   uint8_t* sQ = smem + C::OFF_Q;
   uint8_t* sDO = smem + C::OFF_DO;
-  uint8_t* sRing = smem + C::OFF_RING;
+  uint8_t* sKR = smem + C::OFF_KR;
+  uint8_t* sVR = smem + C::OFF_VR;
 
   const QTileItem it = a.items[blockIdx.x];
   const int nt = (it.reg[0].t_hi - it.reg[0].t_lo) + (it.reg[1].t_hi - it.reg[1].t_lo);
@@ -147,15 +159,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (threadIdx.x == 0) {
     ctl.abort_flag = 0;
     mbar_init(&ctl.q_full, 1);
-    for (int i = 0; i < C::NST; ++i) {
-      mbar_init(&ctl.ring_full[i], 1);
-      mbar_init(&ctl.ring_empty[i], 1);
+    for (int i = 0; i < C::NSK; ++i) {
+      mbar_init(&ctl.k_full[i], 1);
+      mbar_init(&ctl.k_empty[i], 1);
     }
+    for (int i = 0; i < C::NSV; ++i) {
+      mbar_init(&ctl.v_full[i], 1);
+      mbar_init(&ctl.v_empty[i], 1);
+    }
+    mbar_init(&ctl.s_full, 1);
+    mbar_init(&ctl.s_empty, 4 * C::NG);
+    mbar_init(&ctl.dp_empty, 4 * C::NG);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&ctl.s_full[i], 1);
-      mbar_init(&ctl.ds_full[i], 8);
+      mbar_init(&ctl.ds_full[i], 4 * C::NG);
+      mbar_init(&ctl.ds_done[i], 1);
     }
-    mbar_init(&ctl.dp_empty, 8);
     mbar_init(&ctl.acc_done, 1);
     mbar_init(&ctl.drain, 1);
     fence_mbar_init();
@@ -170,7 +188,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = ctl.tmem_base;
 
   if (warp == 0) {
-    // producer: Q and dO once, then K_j, V_j (ring index 2j, 2j+1)
+    // producer: Q and dO once, then K_j (K ring) and V_j (V ring)
     if (lane == 0 && nt > 0) {
       mbar_arrive_expect_tx(&ctl.q_full, 2 * C::Q_BYTES);
       for (int c = 0; c < C::KCH; ++c) {
@@ -178,25 +196,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d(sDO + c * C::BM * 128, &tmDO, &ctl.q_full, c * 64, it.head, it.q_row0);
       }
       bool ok = true;
-      int idx = 0;
-      for (int j = 0; j < nt && ok; ++j) {
+      int j = 0, nk = 0, nv = 0;
+      for (; j < nt && ok; ++j) {
         int r, t;
         qtile_of(it, j, r, t);
         const int key_row = it.reg[r].row0 + t * C::BN;
-        for (int kind = 0; kind < 2; ++kind, ++idx) {
-          const int slot = idx % C::NST;
-          if (!(ok = mbar_wait(&ctl.ring_empty[slot], ((idx / C::NST) & 1) ^ 1, fs))) break;
-          mbar_arrive_expect_tx(&ctl.ring_full[slot], C::TILE_BYTES);
-          uint8_t* dst = sRing + slot * C::TILE_BYTES;
-          const CUtensorMap* tm = kind == 0 ? &tmK : &tmV;
-          for (int c = 0; c < C::KCH; ++c) tma_load_3d(dst + c * C::BN * 128, tm, &ctl.ring_full[slot], c * 64, kvh, key_row);
-        }
+        const int ks = j % C::NSK, vs = j % C::NSV;
+        if (!(ok = mbar_wait(&ctl.k_empty[ks], ((j / C::NSK) & 1) ^ 1, fs))) break;
+        mbar_arrive_expect_tx(&ctl.k_full[ks], C::TILE_BYTES);
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_3d(sKR + ks * C::TILE_BYTES + c * C::BN * 128, &tmK, &ctl.k_full[ks], c * 64, kvh, key_row);
+        ++nk;
+        if (!(ok = mbar_wait(&ctl.v_empty[vs], ((j / C::NSV) & 1) ^ 1, fs))) break;
+        mbar_arrive_expect_tx(&ctl.v_full[vs], C::TILE_BYTES);
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_3d(sVR + vs * C::TILE_BYTES + c * C::BN * 128, &tmV, &ctl.v_full[vs], c * 64, kvh, key_row);
+        ++nv;
       }
       if (!ok) {
         mbar_wait_drain(&ctl.q_full, 0, kWaitLimitNs);
-        for (int back = 1; back <= C::NST && back <= idx; ++back) {
-          const int i2 = idx - back;
-          mbar_wait_drain(&ctl.ring_full[i2 % C::NST], (i2 / C::NST) & 1, kWaitLimitNs);
+        for (int back = 1; back <= C::NSK && back <= nk; ++back) {
+          const int i2 = nk - back;
+          mbar_wait_drain(&ctl.k_full[i2 % C::NSK], (i2 / C::NSK) & 1, kWaitLimitNs);
+        }
+        for (int back = 1; back <= C::NSV && back <= nv; ++back) {
+          const int i2 = nv - back;
+          mbar_wait_drain(&ctl.v_full[i2 % C::NSV], (i2 / C::NSV) & 1, kWaitLimitNs);
         }
       }
     }
@@ -209,31 +234,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t idQ = idesc_bf16(128, D, 0, 1);
       const uint64_t dQd = sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dDOd = sdesc_sw128(smem_u32(sDO), 16, 1024);
-      const uint32_t aRing = smem_u32(sRing);
+      const uint32_t aKR = smem_u32(sKR), aVR = smem_u32(sVR);
       bool ok = mbar_wait(&ctl.q_full, 0, fs);
       tc_fence_after();
       for (int j = 0; j <= nt && ok; ++j) {
         if (j < nt) {
-          const uint32_t b = j & 1;
-          const int ik = 2 * j, iv = 2 * j + 1;
-          if (!(ok = mbar_wait(&ctl.ring_full[ik % C::NST], (ik / C::NST) & 1, fs))) break;
+          const int ks = j % C::NSK, vs = j % C::NSV;
+          if (!(ok = mbar_wait(&ctl.k_full[ks], (j / C::NSK) & 1, fs))) break;
+          // one S buffer: the compute warps must have loaded S_{j-1}
+          if (j >= 1 && !(ok = mbar_wait(&ctl.s_empty, (j - 1) & 1, fs))) break;
           tc_fence_after();
-          const uint64_t kd = sdesc_sw128(aRing + (ik % C::NST) * C::TILE_BYTES, 16, 1024);
-          const uint32_t tS = tmem + C::TM_S + b * C::BN;
+          const uint64_t kd = sdesc_sw128(aKR + ks * C::TILE_BYTES, 16, 1024);
           if (elect_one()) {
 #pragma unroll
             for (int c = 0; c < C::KCH; ++c)
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_bf16_ss(tS, sdesc_add(dQd, c * C::BM * 128 + k * 32), sdesc_add(kd, c * C::BN * 128 + k * 32),
-                            idS, (c | k) != 0);
+                mma_bf16_ss(tmem + C::TM_S, sdesc_add(dQd, c * C::BM * 128 + k * 32),
+                            sdesc_add(kd, c * C::BN * 128 + k * 32), idS, (c | k) != 0);
           }
           __syncwarp();
-          // dP has one buffer: the compute warps must have loaded dP_{j-1}
-          if (!(ok = mbar_wait(&ctl.ring_full[iv % C::NST], (iv / C::NST) & 1, fs))) break;
+          // one dP buffer: the compute warps must have loaded dP_{j-1}
+          if (!(ok = mbar_wait(&ctl.v_full[vs], (j / C::NSV) & 1, fs))) break;
           if (j >= 1 && !(ok = mbar_wait(&ctl.dp_empty, (j - 1) & 1, fs))) break;
           tc_fence_after();
-          const uint64_t vd = sdesc_sw128(aRing + (iv % C::NST) * C::TILE_BYTES, 16, 1024);
+          const uint64_t vd = sdesc_sw128(aVR + vs * C::TILE_BYTES, 16, 1024);
           if (elect_one()) {
 #pragma unroll
             for (int c = 0; c < C::KCH; ++c)
@@ -241,25 +266,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               for (int k = 0; k < 4; ++k)
                 mma_bf16_ss(tmem + C::TM_DP, sdesc_add(dDOd, c * C::BM * 128 + k * 32),
                             sdesc_add(vd, c * C::BN * 128 + k * 32), idS, (c | k) != 0);
-            mma_commit(&ctl.ring_empty[iv % C::NST]);
-            mma_commit(&ctl.s_full[b]);
+            mma_commit(&ctl.v_empty[vs]);
+            mma_commit(&ctl.s_full);
           }
           __syncwarp();
         }
         if (j >= 1) {
-          const int jj = j - 1, ik = 2 * jj;
+          const int jj = j - 1, ks = jj % C::NSK;
           const uint32_t b = jj & 1;
           if (!(ok = mbar_wait(&ctl.ds_full[b], (jj >> 1) & 1, fs))) break;
           tc_fence_after();
-          const uint64_t kmn = sdesc_sw128(aRing + (ik % C::NST) * C::TILE_BYTES, C::BN * 128, 1024);
-          const uint32_t tA = tmem + C::TM_S + b * C::BN;
+          const uint64_t kmn = sdesc_sw128(aKR + ks * C::TILE_BYTES, C::BN * 128, 1024);
+          const uint32_t tA = tmem + C::TM_DS + b * (C::BN / 2);
           const uint32_t acc0 = jj > 0 ? 1u : 0u;
           if (elect_one()) {
 #pragma unroll
             for (int k = 0; k < C::BN / 16; ++k)
-              mma_bf16_ts(tmem + C::TM_DQ, tA + packed_kstep_col64(k), sdesc_add(kmn, k * 16 * 128), idQ,
-                          k > 0 ? 1u : acc0);
-            mma_commit(&ctl.ring_empty[ik % C::NST]);
+              mma_bf16_ts(tmem + C::TM_DQ, tA + 8 * k, sdesc_add(kmn, k * 16 * 128), idQ, k > 0 ? 1u : acc0);
+            mma_commit(&ctl.k_empty[ks]);
+            mma_commit(&ctl.ds_done[b]);
           }
           __syncwarp();
         }
@@ -272,8 +297,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_wait_drain(&ctl.drain, 0, kWaitLimitNs);
     }
   } else {
-    // compute warps: thread <-> query row, half <-> 64 key columns of each 128-key tile
-    const uint32_t wq = warp & 3, half = (warp - 2) >> 2;
+    // compute warps: thread <-> query row, group g <-> 32 key columns of each 128-key tile
+    const uint32_t wq = warp & 3, g = (warp - 2) >> 2;
     const int row = (int)(wq * 32 + lane);
     const uint32_t tl = tmem + ((wq * 32) << 16);
     const int qpos = it.q_pos0 + row;
@@ -288,26 +313,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int r, t;
       qtile_of(it, j, r, t);
       const KeyRegion& kr = it.reg[r];
-      const int kl0 = t * C::BN + 64 * (int)half;
+      const int kl0 = t * C::BN + C::GC * (int)g;
       int lo = 0;
       if (a.window > 0) lo = max(0, qpos - a.window + 1 - kr.pos0);
       const int hi = min(kr.count - 1, qpos - kr.pos0);
-      const int clo = lo - kl0, chi = hi - kl0;  // allowed columns of this half
-      const bool full = (clo <= 0) && (chi >= 63);
-      if (!(ok = mbar_wait(&ctl.s_full[b], (j >> 1) & 1, fs))) break;
+      const int clo = lo - kl0, chi = hi - kl0;  // allowed columns of this group
+      const bool full = (clo <= 0) && (chi >= C::GC - 1);
+      if (!(ok = mbar_wait(&ctl.s_full, j & 1, fs))) break;
       tc_fence_after();
-      uint32_t sr[64], dr[64];
-      tmem_ld32(tl + C::TM_S + b * C::BN + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-      tmem_ld32(tl + C::TM_S + b * C::BN + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
-      tmem_ld32(tl + C::TM_DP + 64 * half, *reinterpret_cast<uint32_t(*)[32]>(&dr[0]));
-      tmem_ld32(tl + C::TM_DP + 64 * half + 32, *reinterpret_cast<uint32_t(*)[32]>(&dr[32]));
+      uint32_t sr[C::GC], dr[C::GC];
+#pragma unroll
+      for (int c4 = 0; c4 < C::GC / 32; ++c4) {
+        tmem_ld32(tl + C::TM_S + C::GC * g + 32 * c4, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c4]));
+        tmem_ld32(tl + C::TM_DP + C::GC * g + 32 * c4, *reinterpret_cast<uint32_t(*)[32]>(&dr[32 * c4]));
+      }
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.dp_empty);
-      uint32_t w[32];
+      if (lane == 0) {
+        mbar_arrive(&ctl.s_empty);
+        mbar_arrive(&ctl.dp_empty);
+      }
+      uint32_t w[C::GC / 2];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
+      for (int e = 0; e < C::GC / 2; ++e) {
         const int c = 2 * e;
         float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2));
         float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, -lse2));
@@ -317,7 +346,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         w[e] = pack_bf16x2(p0 * (__uint_as_float(dr[c]) - delta), p1 * (__uint_as_float(dr[c + 1]) - delta));
       }
-      tmem_st32(tl + C::TM_S + b * C::BN + 64 * half, w);
+      // the dS buffer is free once the dQ MMAs of tile j-2 have completed
+      if (j >= 2 && !(ok = mbar_wait(&ctl.ds_done[b], ((j - 2) >> 1) & 1, fs))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c4 = 0; c4 < C::GC / 32; ++c4)
+        tmem_st16(tl + C::TM_DS + b * (C::BN / 2) + (C::GC / 2) * g + 16 * c4,
+                  *reinterpret_cast<const uint32_t(*)[16]>(&w[16 * c4]));
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -327,10 +362,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = mbar_wait(&ctl.acc_done, 0, fs);
       tc_fence_after();
       if (ok) {
+        // this warp writes dQ columns [g * D / NG, (g + 1) * D / NG) of its rows
+        constexpr int OC = D / C::NG;
         __nv_bfloat16* qrow = a.dq + ((int64_t)(it.q_row0 + row) * a.Hq + it.head) * D;
 #pragma unroll
-        for (int c4 = 0; c4 < D / 64; ++c4) {
-          const int col = (int)half * (D / 2) + c4 * 32;
+        for (int c4 = 0; c4 < (OC + 31) / 32; ++c4) {
+          const int col = (int)g * OC + c4 * 32;
           uint32_t rr[32];
           tmem_ld32(tl + C::TM_DQ + col, rr);
           tmem_ld_wait();
@@ -341,7 +378,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(qrow + col);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+            for (int v = 0; v < OC / 8 && v < 4; ++v) dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
           }
         }
       }
@@ -729,14 +766,15 @@ cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st) {
 
 template <int D, typename Cfg, typename K, typename Args>
 static cudaError_t launch_tc(K kernel, const CUtensorMap& t0, const CUtensorMap& t1, const CUtensorMap& t2,
-                             const CUtensorMap& t3, const Args& a, int n_items, cudaStream_t st) {
+                             const CUtensorMap& t3, const Args& a, int n_items, cudaStream_t st,
+                             int threads = kBwdThreads) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kernel<<<n_items, kBwdThreads, Cfg::SMEM_BYTES, st>>>(t0, t1, t2, t3, a);
+  kernel<<<n_items, threads, Cfg::SMEM_BYTES, st>>>(t0, t1, t2, t3, a);
   return cudaGetLastError();
 }
 
@@ -745,9 +783,9 @@ cudaError_t launch_dq(int D, const CUtensorMap& tq, const CUtensorMap& tk, const
   if (n_items <= 0) return cudaSuccess;
   switch (D) {
     case 64:
-      return launch_tc<64, DqCfg<64>>(dq_kernel<64>, tq, tk, tv, tdo, a, n_items, st);
+      return launch_tc<64, DqCfg<64>>(dq_kernel<64>, tq, tk, tv, tdo, a, n_items, st, DqCfg<64>::THREADS);
     case 128:
-      return launch_tc<128, DqCfg<128>>(dq_kernel<128>, tq, tk, tv, tdo, a, n_items, st);
+      return launch_tc<128, DqCfg<128>>(dq_kernel<128>, tq, tk, tv, tdo, a, n_items, st, DqCfg<128>::THREADS);
     default:
       return cudaErrorInvalidValue;
   }

@@ -7,7 +7,7 @@
 // (prompt) and then region 1 (own segment), clipped to the causal / window
 // range, with an online softmax.
 //
-// Warp roles (192 threads):
+// Warp roles (64 + 128 * NH threads):
 //   warp 0      TMA producer: the Q tile once, then K and V tiles through a
 //               ring of "units" (128 rows x 128 head-dim columns, two 64-column
 //               TMA boxes) in the order the MMA warp consumes them
@@ -15,11 +15,16 @@
 //   warp 1      TMEM owner and MMA issuer (whole warp, one elected lane issues):
 //               S_j = Q K_j^T (A and B in shared memory) into one of two TMEM
 //               S buffers; O += P_{j-1} V_{j-1} with P read from TMEM
-//   warps 2-5   softmax: thread <-> query row (TMEM lane); reads S_j, masks,
-//               keeps the running max m and sum l (log2 units), writes P_j as
-//               packed bf16 over the first 64 columns of S_j's own buffer,
-//               rescales O in TMEM when m grows by more than 2^8 (exact: O and
-//               l share the stale max), finally writes out = O / l and lse.
+//   warps 2..    softmax: thread <-> query row (TMEM lane).  With NH = 2 (head
+//               dimension <= 128) each row's 128 key columns are split over two
+//               warps ("halves"); each half keeps its own running max m and sum
+//               l (log2 units) and its own O accumulator in TMEM (PV runs as two
+//               K = 64 GEMMs), so the halves never wait on each other inside the
+//               key walk.  A half reads S_j columns [64h, 64h+64), masks, writes
+//               P_j as packed bf16 over the first 32 of those columns, and
+//               rescales its O when its m grows by more than 2^8 (exact: O and l
+//               share the stale max).  The epilogue combines the halves:
+//               out = (O_0 2^(m_0-m) + O_1 2^(m_1-m)) / (l_0 2^(m_0-m) + l_1 2^(m_1-m)).
 // tcgen05.mma ops issued by one thread execute in issue order, so S_{j+2} is
 // written into the buffer holding P_j only after PV_j, which reads it.
 //
@@ -39,6 +44,9 @@ template <int D>
 struct FwdCfg {
   static constexpr int BM = 128, BN = 128;
   static constexpr int NSPLIT = (D == 512) ? 2 : 1;
+  static constexpr int NH = (D == 512) ? 1 : 2;        // key-column halves per row
+  static constexpr int HC = BN / NH;                   // key columns of one half
+  static constexpr int THREADS = 64 + 128 * NH;
   static constexpr int DV = D / NSPLIT;                // output columns of one CTA
   static constexpr int QCH = D / 64;                   // 64-column chunks of Q / K
   static constexpr int UCH = (D == 64) ? 1 : 2;        // chunks per ring unit
@@ -51,7 +59,7 @@ struct FwdCfg {
   static constexpr int OFF_RING = Q_BYTES;
   static constexpr int SMEM_BYTES = OFF_RING + NST * UNIT_BYTES + 1024;  // + alignment slack
   static constexpr uint32_t TM_S = 0;                  // S buffers at columns 0 and BN
-  static constexpr uint32_t TM_O = 2 * BN;             // O accumulator (DV columns)
+  static constexpr uint32_t TM_O = 2 * BN;             // O accumulators, one per half (DV columns each)
   static constexpr uint32_t TM_COLS = 512;
   static constexpr float RESCALE_THRESHOLD = 8.0f;     // log2 units
 };
@@ -61,6 +69,7 @@ struct FwdSmemCtl {
   uint64_t ring_full[12], ring_empty[12];
   uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t drain;
+  uint64_t pair_done[4];      // per lane quarter: both halves have published (m, l)
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -77,7 +86,7 @@ __device__ __forceinline__ void tile_of(const QTileItem& it, int j, int& r, int&
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
   using C = FwdCfg<D>;
@@ -104,9 +113,10 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl.s_full[i], 1);
-      mbar_init(&ctl.p_full[i], 4);
+      mbar_init(&ctl.p_full[i], 4 * C::NH);
       mbar_init(&ctl.pv_done[i], 1);
     }
+    for (int i = 0; i < 4; ++i) mbar_init(&ctl.pair_done[i], 32 * C::NH);
     mbar_init(&ctl.drain, 1);
     fence_mbar_init();
   }
@@ -205,11 +215,13 @@ __global__ void __launch_bounds__(192, 1)
             if (!(ok = mbar_wait(&ctl.ring_full[slot], (idx / C::NST) & 1, fs))) break;
             tc_fence_after();
             const uint64_t vdesc = sdesc_sw128(aRing + slot * C::UNIT_BYTES, C::BN * 128, 1024);
-            const uint32_t tO = tmem + C::TM_O + u * C::UCH * 64;
             if (elect_one()) {
 #pragma unroll
-              for (int k = 0; k < C::BN / 16; ++k)
-                mma_bf16_ts(tO, tP + k * 8, sdesc_add(vdesc, k * 16 * 128), idO, k > 0 ? 1u : acc0);
+              for (int h = 0; h < C::NH; ++h)
+#pragma unroll
+                for (int k = 0; k < C::HC / 16; ++k)
+                  mma_bf16_ts(tmem + C::TM_O + h * C::DV + u * C::UCH * 64, tP + h * C::HC + k * 8,
+                              sdesc_add(vdesc, (h * C::HC + k * 16) * 128), idO, k > 0 ? 1u : acc0);
               mma_commit(&ctl.ring_empty[slot]);
               if (u == C::VU - 1) mma_commit(&ctl.pv_done[b]);
             }
@@ -225,8 +237,10 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // ------------------------------------------------------------ softmax
     const uint32_t wq = warp & 3;
+    const int half = (int)((warp - 2) >> 2);  // 0 .. NH-1
     const int row = (int)(wq * 32 + lane);
     const uint32_t tl = tmem + ((wq * 32) << 16);
+    const uint32_t tO = tl + C::TM_O + half * C::DV;
     const int qpos = it.q_pos0 + row;
     const float sl2 = a.scale_log2;
     float m = -INFINITY, l = 0.f;
@@ -236,20 +250,20 @@ __global__ void __launch_bounds__(192, 1)
       int r, t;
       tile_of(it, j, r, t);
       const KeyRegion& kr = it.reg[r];
-      const int kl0 = t * C::BN;  // local index of the tile's first key in its region
+      const int kl0 = t * C::BN + half * C::HC;  // local index of this half's first key
       int lo = 0;
       if (a.window > 0) lo = max(0, qpos - a.window + 1 - kr.pos0);
       const int hi = min(kr.count - 1, qpos - kr.pos0);
-      const int clo = lo - kl0, chi = hi - kl0;  // allowed columns [clo, chi]
-      const bool full = (clo <= 0) && (chi >= C::BN - 1);
+      const int clo = lo - kl0, chi = hi - kl0;  // allowed columns [clo, chi] of this half
+      const bool full = (clo <= 0) && (chi >= C::HC - 1);
       if (!(ok = mbar_wait(&ctl.s_full[b], (j >> 1) & 1, fs))) break;
       tc_fence_after();
 
-      float s[C::BN];
+      float s[C::HC];
 #pragma unroll
-      for (int c4 = 0; c4 < C::BN / 32; ++c4) {
+      for (int c4 = 0; c4 < C::HC / 32; ++c4) {
         uint32_t rr[32];
-        tmem_ld32(tl + C::TM_S + b * C::BN + c4 * 32, rr);
+        tmem_ld32(tl + C::TM_S + b * C::BN + half * C::HC + c4 * 32, rr);
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[c4 * 32 + i] = __uint_as_float(rr[i]);
       }
@@ -258,10 +272,10 @@ __global__ void __launch_bounds__(192, 1)
       float mx = -INFINITY;
       if (full) {
 #pragma unroll
-        for (int c = 0; c < C::BN; ++c) mx = fmaxf(mx, s[c]);
+        for (int c = 0; c < C::HC; ++c) mx = fmaxf(mx, s[c]);
       } else {
 #pragma unroll
-        for (int c = 0; c < C::BN; ++c) {
+        for (int c = 0; c < C::HC; ++c) {
           s[c] = (c < clo || c > chi) ? -INFINITY : s[c];
           mx = fmaxf(mx, s[c]);
         }
@@ -279,11 +293,11 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
         for (int c4 = 0; c4 < C::DV / 32; ++c4) {
           uint32_t rr[32];
-          tmem_ld32(tl + C::TM_O + c4 * 32, rr);
+          tmem_ld32(tO + c4 * 32, rr);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-          tmem_st32(tl + C::TM_O + c4 * 32, rr);
+          tmem_st32(tO + c4 * 32, rr);
         }
         tmem_st_wait();
         l *= alpha;
@@ -292,17 +306,17 @@ __global__ void __launch_bounds__(192, 1)
       const float m_use = (m == -INFINITY) ? 0.f : m;
       float sum = 0.f;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h2 = 0; h2 < C::HC / 64; ++h2) {
         uint32_t w[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const int c = h * 64 + 2 * e;
+          const int c = h2 * 64 + 2 * e;
           const float p0 = ex2_approx(fmaf(s[c], sl2, -m_use));
           const float p1 = ex2_approx(fmaf(s[c + 1], sl2, -m_use));
           sum += p0 + p1;
           w[e] = pack_bf16x2(p0, p1);
         }
-        tmem_st32(tl + C::TM_S + b * C::BN + h * 32, w);
+        tmem_st32(tl + C::TM_S + b * C::BN + half * C::HC + h2 * 32, w);
       }
       l += sum;
       tmem_st_wait();
@@ -311,32 +325,60 @@ __global__ void __launch_bounds__(192, 1)
       if (lane == 0) mbar_arrive(&ctl.p_full[b]);
     }
     if (ok && nt > 0) {
-      // epilogue: out = O / l, lse = (m + log2 l) ln 2
+      // epilogue: combine the halves, out = O / l, lse = (m + log2 l) ln 2
       ok = mbar_wait(&ctl.pv_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, fs);
       tc_fence_after();
+      float mh[2] = {m, -INFINITY}, lh[2] = {l, 0.f};
+      if (ok && C::NH == 2) {
+        // the K/V ring is idle once the last PV has completed: borrow 2 KB of it
+        float* half_m = reinterpret_cast<float*>(sRing);  // [2][128]
+        float* half_l = half_m + 256;                      // [2][128]
+        half_m[half * 128 + row] = m;
+        half_l[half * 128 + row] = l;
+        mbar_arrive(&ctl.pair_done[wq]);
+        ok = mbar_wait(&ctl.pair_done[wq], 0, fs);
+        mh[0] = half_m[row];
+        mh[1] = half_m[128 + row];
+        lh[0] = half_l[row];
+        lh[1] = half_l[128 + row];
+      }
       if (ok) {
         const bool valid = row < it.q_rows;
-        const float inv_l = 1.f / l;
-        __nv_bfloat16* orow = a.out + ((int64_t)(it.q_row0 + row) * a.Hq + it.head) * D + split * C::DV;
+        const float mtot = fmaxf(mh[0], mh[1]);
+        const float mref = (mtot == -INFINITY) ? 0.f : mtot;
+        const float f0 = (mh[0] == -INFINITY) ? 0.f : ex2_approx(mh[0] - mref);
+        const float f1 = (mh[1] == -INFINITY) ? 0.f : ex2_approx(mh[1] - mref);
+        const float ltot = lh[0] * f0 + lh[1] * f1;
+        const float inv_l = 1.f / ltot;
+        const float g0 = f0 * inv_l, g1 = f1 * inv_l;
+        // this warp writes output columns [half * DV / NH, ...) of its rows
+        constexpr int OC = C::DV / C::NH;
+        __nv_bfloat16* orow = a.out + ((int64_t)(it.q_row0 + row) * a.Hq + it.head) * D + split * C::DV + half * OC;
 #pragma unroll
-        for (int c4 = 0; c4 < C::DV / 32; ++c4) {
-          uint32_t rr[32];
-          tmem_ld32(tl + C::TM_O + c4 * 32, rr);
+        for (int c4 = 0; c4 < OC / 32; ++c4) {
+          const int col = half * OC + c4 * 32;
+          uint32_t r0[32], r1[32];
+          tmem_ld32(tl + C::TM_O + col, r0);
+          if (C::NH == 2) tmem_ld32(tl + C::TM_O + C::DV + col, r1);
           tmem_ld_wait();
           uint32_t w[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * inv_l, __uint_as_float(rr[2 * i + 1]) * inv_l);
+          for (int i = 0; i < 16; ++i) {
+            float x0 = __uint_as_float(r0[2 * i]) * g0, x1 = __uint_as_float(r0[2 * i + 1]) * g0;
+            if (C::NH == 2) {
+              x0 = fmaf(__uint_as_float(r1[2 * i]), g1, x0);
+              x1 = fmaf(__uint_as_float(r1[2 * i + 1]), g1, x1);
+            }
+            w[i] = pack_bf16x2(x0, x1);
+          }
           if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c4 * 32);
 #pragma unroll
             for (int v = 0; v < 4; ++v) dst[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
           }
         }
-        if (valid && split == 0) {
-          const float m_use = (m == -INFINITY) ? 0.f : m;
-          a.lse[(int64_t)it.head * a.T + it.q_row0 + row] = (m_use + __log2f(l)) * 0.69314718055994530942f;
-        }
+        if (valid && split == 0 && half == 0)
+          a.lse[(int64_t)it.head * a.T + it.q_row0 + row] = (mref + __log2f(ltot)) * 0.69314718055994530942f;
       }
     }
   }
@@ -359,7 +401,7 @@ static cudaError_t launch_fwd_d(const CUtensorMap& tq, const CUtensorMap& tk, co
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  fwd_kernel<D><<<n_items * C::NSPLIT, 192, C::SMEM_BYTES, st>>>(tq, tk, tv, a);
+  fwd_kernel<D><<<n_items * C::NSPLIT, C::THREADS, C::SMEM_BYTES, st>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
 
