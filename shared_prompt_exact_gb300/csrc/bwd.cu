@@ -334,16 +334,18 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         mbar_arrive(&ctl.s_empty);
         mbar_arrive(&ctl.dp_empty);
       }
+      // masked keys get S = -inf once (exp2 gives 0); tiles with no masked key skip this
+      if (!full) {
+#pragma unroll
+        for (int c = 0; c < C::GC; ++c)
+          if (c < clo || c > chi) sr[c] = __float_as_uint(-INFINITY);
+      }
       uint32_t w[C::GC / 2];
 #pragma unroll
       for (int e = 0; e < C::GC / 2; ++e) {
         const int c = 2 * e;
-        float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2));
-        float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, -lse2));
-        if (!full) {
-          p0 = (c < clo || c > chi) ? 0.f : p0;
-          p1 = (c + 1 < clo || c + 1 > chi) ? 0.f : p1;
-        }
+        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, -lse2));
         w[e] = pack_bf16x2(p0 * (__uint_as_float(dr[c]) - delta), p1 * (__uint_as_float(dr[c + 1]) - delta));
       }
       // the dS buffer is free once the dQ MMAs of tile j-2 have completed
@@ -617,6 +619,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const float4* L4 = reinterpret_cast<const float4*>(&ctl.lse2[slot][32 * half]);
       const float4* D4 = reinterpret_cast<const float4*>(&ctl.delta[slot][32 * half]);
       tmem_ld_wait();
+      // masked queries get S = -inf once (exp2 gives 0); blocks with no masked query skip this
+      if (!full) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (c < clo || c > chi) sr[c] = __float_as_uint(-INFINITY);
+      }
       uint32_t wp[16], ws[16];
 #pragma unroll
       for (int e4 = 0; e4 < 8; ++e4) {
@@ -625,12 +633,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int c = 4 * e4 + 2 * e2;
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lv[2 * e2]));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, -lv[2 * e2 + 1]));
-          if (!full) {
-            p0 = (c < clo || c > chi) ? 0.f : p0;
-            p1 = (c + 1 < clo || c + 1 > chi) ? 0.f : p1;
-          }
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lv[2 * e2]));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, -lv[2 * e2 + 1]));
           wp[2 * e4 + e2] = pack_bf16x2(p0, p1);
           ws[2 * e4 + e2] = pack_bf16x2(p0 * (__uint_as_float(dr[c]) - dv[2 * e2]),
                                         p1 * (__uint_as_float(dr[c + 1]) - dv[2 * e2 + 1]));
