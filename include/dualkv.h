@@ -91,9 +91,11 @@ size_t dualkv_bwd_workspace_bytes(int P, int N, const int32_t* R_offsets, int Hq
  * gather the contributions of every segment, since the packed result equals
  * standard attention on the replicated sequences with prompt gradients summed).
  * Runs: preprocess (Delta = rowsum(dout * out)), dK/dV (each key tile walks
- * every query block that attends it in a fixed order: group heads ascending,
- * prompt query blocks ascending, then segments 0..N-1 ascending), a
- * fixed-order reduction of split prompt tiles, and dQ.
+ * every query block that attends it in a fixed order: for a prompt key tile the
+ * blocks of segments 0..N-1 and then of the prompt, ascending; the group's
+ * heads of one block consecutively), a fixed-order reduction of split prompt
+ * tiles, and dQ.  For D = 512 the dK/dV and dQ products are formed from bf16
+ * P and dS blocks kept in the workspace (see dualkv_bwd_workspace_bytes).
  *
  *   q, k, v, out, lse, dout   as produced for/by dualkv_fwd with the same layout
  *   dq, dk, dv                device bf16, written

@@ -11,8 +11,10 @@
 // the replicated prompt gradients.
 //
 // Kernels: prep (Delta and log2-scaled LSE), dkv (one CTA per key tile and
-// chunk of its query walk; fixed walk order), reduce (fixed-order sum of split
-// chunks), dq (one CTA per query tile; same key walk as the forward).
+// chunk of its query walk; fixed walk order: for a prompt key tile every
+// segment's query blocks, then the prompt's; the group's heads of one block
+// consecutively), reduce (fixed-order sum of split chunks), dq (one CTA per
+// query tile; same key walk as the forward).
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -481,8 +483,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // values of block i, fetched one iteration ahead
       auto fetch = [&](int idx, int& h, QBlock& qb, float (&l2)[2], float (&dl)[2]) {
         const int itx = it.it_lo + idx;
-        h = it.kv_head * gs + itx / it.list_len;
-        qb = a.qblocks[it.list_begin + itx % it.list_len];
+        h = it.kv_head * gs + itx % gs;
+        qb = a.qblocks[it.list_begin + itx / gs];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int c = (int)lane + 32 * e;

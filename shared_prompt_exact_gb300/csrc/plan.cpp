@@ -115,9 +115,17 @@ KVPlan plan_kvtiles(const Layout& L, int key_tile, int q_block, int max_iters) {
     for (int a = 0; a < k.count; a += key_tile) {
       TileList tl{k.row0 + a, k.pos0 + a, std::min(key_tile, k.count - a), (int32_t)plan.qblocks.size(), 0};
       const int kp_first = tl.k_pos0, kp_last = tl.k_pos0 + tl.k_rows - 1;
-      // query regions that see region kr: all of them for the prompt, else its own
-      const size_t q_lo = kr == 0 ? 0 : kr, q_hi = kr == 0 ? regs.size() : kr + 1;
-      for (size_t qr = q_lo; qr < q_hi; ++qr) {
+      // query regions that see region kr: its own for a segment; for the prompt, every
+      // segment (0..N-1) first and then the prompt itself, so that the long common part
+      // of all prompt key tiles' walks comes first and lines up across tiles (L2 reuse)
+      std::vector<size_t> qorder;
+      if (kr == 0) {
+        for (size_t qr = 1; qr < regs.size(); ++qr) qorder.push_back(qr);
+        qorder.push_back(0);
+      } else {
+        qorder.push_back(kr);
+      }
+      for (size_t qr : qorder) {
         const Region& q = regs[qr];
         if (q.count <= 0) continue;
         int64_t lo = std::max<int64_t>(kp_first, q.pos0);
@@ -132,14 +140,18 @@ KVPlan plan_kvtiles(const Layout& L, int key_tile, int q_block, int max_iters) {
       tiles.push_back(tl);
     }
   }
-  for (int g = 0; g < L.Hkv; ++g)
+  // Chunks are emitted split-major (chunk s of every key tile of a kv-head, then
+  // chunk s+1): CTAs that run together then stream the same query blocks.
+  for (int g = 0; g < L.Hkv; ++g) {
+    std::vector<std::vector<KVTileItem>> per_tile;
+    int max_split = 0;
     for (const TileList& tl : tiles) {
       const int total = gs * tl.len;
       const int nsplit = std::max(1, (total + max_iters - 1) / max_iters);
       const int chunk = (total + nsplit - 1) / nsplit;
       const int slot0 = plan.nslots;
-      int made = 0;
-      for (int lo = 0; lo < total; lo += chunk, ++made) {
+      std::vector<KVTileItem> mine;
+      for (int lo = 0; lo < total; lo += chunk) {
         KVTileItem it{};
         it.k_row0 = tl.k_row0;
         it.k_pos0 = tl.k_pos0;
@@ -150,12 +162,19 @@ KVPlan plan_kvtiles(const Layout& L, int key_tile, int q_block, int max_iters) {
         it.it_lo = lo;
         it.it_hi = std::min(total, lo + chunk);
         it.partial_slot = nsplit > 1 ? plan.nslots++ : -1;
-        plan.items.push_back(it);
+        mine.push_back(it);
       }
-      if (nsplit > 1) plan.reduces.push_back(ReduceItem{tl.k_row0, tl.k_rows, g, slot0, made, 0});
+      if (nsplit > 1) plan.reduces.push_back(ReduceItem{tl.k_row0, tl.k_rows, g, slot0, (int)mine.size(), 0});
+      max_split = std::max(max_split, (int)mine.size());
+      per_tile.push_back(std::move(mine));
     }
+    for (int sidx = 0; sidx < max_split; ++sidx)
+      for (const auto& mine : per_tile)
+        if (sidx < (int)mine.size()) plan.items.push_back(mine[sidx]);
+  }
+  // heaviest first, on a coarse cost bucket so that equal-sized chunks keep their split-major order
   std::stable_sort(plan.items.begin(), plan.items.end(), [](const KVTileItem& a, const KVTileItem& b) {
-    return (a.it_hi - a.it_lo) > (b.it_hi - b.it_lo);
+    return (a.it_hi - a.it_lo) / 64 > (b.it_hi - b.it_lo) / 64;
   });
   return plan;
 }

@@ -35,8 +35,9 @@ struct QBlock {
 };
 
 // dK/dV work item: one key tile of one kv-head, walking iterations
-// [it_lo, it_hi) of the tile's query list.  Iteration `it` is group head
-// it / list_len and query block qblocks[list_begin + it % list_len].
+// [it_lo, it_hi) of the tile's query list.  Iteration `it` is query block
+// qblocks[list_begin + it / G] of group head it % G (G = Hq / Hkv): the group's
+// heads of one block are consecutive.
 struct KVTileItem {
   int32_t k_row0, k_pos0, k_rows, kv_head;
   int32_t list_begin, list_len;
