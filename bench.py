@@ -262,6 +262,48 @@ def run_reference(args, w):
     return 0
 
 
+# ------------------------------------------------------------------ tensor packing
+def measure_packing(w, dev, stream, reps):
+    """dualkv_pack / dualkv_unpack / dualkv_fold on hidden-size rows (Hq * D bf16)
+    of the workload's layout; each call timed alone with CUDA events on the
+    launching stream.  Algorithmic bytes: every source row the definition needs
+    read once, every destination row written once."""
+    from shared_prompt_exact_gb300 import dualkv
+    E = w.Hq * w.D
+    T, T_rep = w.T, w.T_replicated
+    row = 2 * E
+    gen = torch.Generator(device=dev).manual_seed(w.seed + 7)
+    x_rep = torch.randn(T_rep, E, generator=gen, device=dev).to(torch.bfloat16)
+    x_pk = torch.empty(T, E, dtype=torch.bfloat16, device=dev)
+    ops = {
+        "pack": (lambda: dualkv.dualkv_pack(x_rep, x_pk, w.P, w.N, w.offsets, stream), 2 * T * row),
+        "unpack": (lambda: dualkv.dualkv_unpack(x_pk, x_rep, w.P, w.N, w.offsets, stream), (T + T_rep) * row),
+        "fold": (lambda: dualkv.dualkv_fold(x_rep, x_pk, w.P, w.N, w.offsets, stream), (T_rep + T) * row),
+    }
+    hbm = peaks()
+    res = {"row_elems": E, "packed_rows": T, "replicated_rows": T_rep,
+           "l2": "no flush: each call moves more than L2 (%.2f GB replicated)" % (T_rep * row / 1e9)}
+    for name, (fn, nbytes) in ops.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / reps
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"ms": ms, "algorithmic_bytes": nbytes, "GB/s": gbs, "frac_hbm": gbs / hbm["hbm_gbs"],
+                     "peak_source": hbm["source"] + " copy bandwidth"}
+    dualkv.dualkv_check_status(stream)
+    del x_rep, x_pk
+    torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_dualkv(args, w):
     from shared_prompt_exact_gb300 import build as pbuild
@@ -403,6 +445,10 @@ def run_dualkv(args, w):
                       "speedup_packed_over_replicated": ms_rep / ms_step}
         del qr, kr, vr, dor, outr, dqr, dkr, dvr, wsr
 
+    packing = None
+    if not args.no_pack:
+        packing = measure_packing(w, dev, stream, max(3, min(args.steps, 10)))
+
     sampler.stop()
     clocks = sampler.summary(t_start, t_end)
 
@@ -435,6 +481,7 @@ def run_dualkv(args, w):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "replicated": replicated,
+            "tensor_packing": packing,
             "gpu_launches": int(round(launches_per_step * args.steps)),
             "clocks": clocks,
         }
@@ -458,6 +505,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-replicated", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-pack", action="store_true", help="skip the pack/unpack/fold measurement")
     args = ap.parse_args(argv)
     w = wl.WORKLOADS[args.config]
     if args.heads:

@@ -118,6 +118,42 @@ int dualkv_build_index(int P, int N, const int32_t* R_offsets, int32_t* seg_id, 
                        int32_t* cu_seqlens_rep, int32_t* rep2pack);
 
 /*
+ * Per-token tensors between the replicated and the packed layout (paper
+ * abstract: the pipeline repacks the N(P+R) tokens into P+NR, which extends the
+ * token reduction from attention to the whole model; these calls move the
+ * activations and gradients of the layers around attention).
+ *
+ * Replicated layout: sequence n is the P prompt rows followed by its R_n
+ * response rows; the sequences lie end to end (sequence n starts at row
+ * n*P + R_offsets[n]; T_rep = N*P + R_offsets[N] rows).  Packed layout as
+ * above (T rows).  A row is row_elems bf16 values (row_elems >= 8, a multiple
+ * of 8, i.e. whole 16-byte vectors), rows contiguous, both buffers device
+ * memory, 16-byte aligned, owned by the caller, and not overlapping.
+ *
+ *   dualkv_pack    x_rep[T_rep, row] -> x_packed[T, row]: a prompt row is
+ *                  copied from replica 0, a response row from its sequence.
+ *   dualkv_unpack  x_packed[T, row] -> x_rep[T_rep, row]: every replica gets
+ *                  a copy of the prompt rows (the inverse of pack on tensors
+ *                  whose replicas agree).
+ *   dualkv_fold    g_rep[T_rep, row] -> g_packed[T, row]: the adjoint of
+ *                  unpack, i.e. the gradient of the packed rows.  A prompt row
+ *                  is the sum of its N replica rows, accumulated in fp32 in
+ *                  replica order n = 0..N-1 and rounded once to bf16; a
+ *                  response row is copied.
+ *
+ * Copies are bit-exact.  Asynchronous on `stream`.  Returns DUALKV_OK,
+ * DUALKV_ERR_INVALID (bad layout, row_elems, null or overlapping buffers),
+ * DUALKV_ERR_ALIGN or DUALKV_ERR_CUDA.  The first call for a layout uploads
+ * R_offsets into a small cached device array (freed by dualkv_release()).
+ */
+int dualkv_pack(const void* x_rep, void* x_packed, int P, int N, const int32_t* R_offsets, int row_elems,
+                void* stream);
+int dualkv_unpack(const void* x_packed, void* x_rep, int P, int N, const int32_t* R_offsets, int row_elems,
+                  void* stream);
+int dualkv_fold(const void* g_rep, void* g_packed, int P, int N, const int32_t* R_offsets, int row_elems,
+                void* stream);
+
+/*
  * Token-reduction factor rho = sum_n (P + R_n) / (P + sum_n R_n) (paper
  * abstract: rho = N(P+R)/(P+NR) for equal lengths).  Host only; -1 on invalid input.
  */
@@ -153,7 +189,8 @@ const char* dualkv_error_string(int code);
 #define DUALKV_KERNEL_DKV 2
 #define DUALKV_KERNEL_REDUCE 3
 #define DUALKV_KERNEL_DQ 4
-#define DUALKV_KERNEL_KINDS 5
+#define DUALKV_KERNEL_PACK 5 /* dualkv_pack, dualkv_unpack and dualkv_fold */
+#define DUALKV_KERNEL_KINDS 6
 int dualkv_profile_enable(int on);
 int dualkv_profile_read(double* ms, int64_t* launches);
 

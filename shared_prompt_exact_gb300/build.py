@@ -16,7 +16,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libdualkv.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["fwd.cu", "bwd.cu", "bwd512.cu", "api.cu", "noalloc.cu", "plan.cpp"]
+SOURCES = ["fwd.cu", "bwd.cu", "bwd512.cu", "api.cu", "noalloc.cu", "pack.cu", "plan.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr", "-I", INCLUDE]

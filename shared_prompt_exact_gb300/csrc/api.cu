@@ -64,6 +64,13 @@ struct DevPlan {
 };
 std::map<std::string, std::unique_ptr<DevPlan>> g_plans;
 
+struct DevOffsets {
+  int32_t* d = nullptr;
+  int num_sms = 0;
+  ~DevOffsets() { cudaFree(d); }
+};
+std::map<std::string, std::unique_ptr<DevOffsets>> g_offsets;  // (device, P, N, R_offsets) -> device copy
+
 std::string plan_key(int device, int P, int N, const int32_t* off, int Hq, int Hkv, int D, int window) {
   std::string k;
   k.reserve(64 + 4 * (N + 1));
@@ -232,6 +239,50 @@ int make_block_tmap(CUtensorMap* m, const void* base, int64_t n_blocks, int box_
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DUALKV_OK : DUALKV_ERR_CUDA;
+}
+
+// Device copy of R_offsets and the SM count for the pack kernels; caller holds g_mu.
+int get_offsets(int P, int N, const int32_t* off, DevOffsets** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DUALKV_ERR_CUDA;
+  auto& slot = g_offsets[plan_key(dev, P, N, off, 0, 0, 0, 0)];
+  if (!slot) {
+    std::unique_ptr<DevOffsets> o(new DevOffsets());
+    if (cudaDeviceGetAttribute(&o->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return DUALKV_ERR_CUDA;
+    if (upload(&o->d, std::vector<int32_t>(off, off + N + 1)) != cudaSuccess) return DUALKV_ERR_CUDA;
+    slot = std::move(o);
+  }
+  *out = slot.get();
+  return DUALKV_OK;
+}
+
+// Shared checks and launch of dualkv_pack / dualkv_unpack / dualkv_fold.
+int pack_call(int kind, const void* src, void* dst, int P, int N, const int32_t* off, int row_elems, void* stream) {
+  if (P < 0 || N < 1 || !off || off[0] != 0) return DUALKV_ERR_INVALID;
+  for (int n = 0; n < N; ++n)
+    if (off[n + 1] < off[n]) return DUALKV_ERR_INVALID;
+  const int64_t T = (int64_t)P + off[N];
+  const int64_t T_rep = (int64_t)N * P + off[N];
+  if (T < 1 || T_rep > INT32_MAX) return DUALKV_ERR_INVALID;
+  if (row_elems < 8 || row_elems % 8) return DUALKV_ERR_INVALID;
+  if (!src || !dst) return DUALKV_ERR_INVALID;
+  if (!aligned16(src) || !aligned16(dst)) return DUALKV_ERR_ALIGN;
+  const uint64_t row_bytes = (uint64_t)row_elems * 2;
+  const uint64_t src_bytes = row_bytes * (uint64_t)(kind == 1 ? T : T_rep);
+  const uint64_t dst_bytes = row_bytes * (uint64_t)(kind == 1 ? T_rep : T);
+  const uint64_t s0 = reinterpret_cast<uintptr_t>(src), d0 = reinterpret_cast<uintptr_t>(dst);
+  if (s0 < d0 + dst_bytes && d0 < s0 + src_bytes) return DUALKV_ERR_INVALID;  // overlapping buffers
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevOffsets* o = nullptr;
+  int rc = get_offsets(P, N, off, &o);
+  if (rc) return rc;
+  if (timed(DUALKV_KERNEL_PACK, st, [&] {
+        return launch_pack(kind, src, dst, o->d, P, N, T, row_elems, o->num_sms, st);
+      }) != cudaSuccess)
+    return DUALKV_ERR_CUDA;
+  return DUALKV_OK;
 }
 
 bool supported_d(int D) { return D == 64 || D == 128 || D == 512; }  // backward
@@ -406,6 +457,21 @@ int64_t dualkv_pairs(int P, int N, const int32_t* R_offsets, int window) {
   return total;
 }
 
+int dualkv_pack(const void* x_rep, void* x_packed, int P, int N, const int32_t* R_offsets, int row_elems,
+                void* stream) {
+  return pack_call(0, x_rep, x_packed, P, N, R_offsets, row_elems, stream);
+}
+
+int dualkv_unpack(const void* x_packed, void* x_rep, int P, int N, const int32_t* R_offsets, int row_elems,
+                  void* stream) {
+  return pack_call(1, x_packed, x_rep, P, N, R_offsets, row_elems, stream);
+}
+
+int dualkv_fold(const void* g_rep, void* g_packed, int P, int N, const int32_t* R_offsets, int row_elems,
+                void* stream) {
+  return pack_call(2, g_rep, g_packed, P, N, R_offsets, row_elems, stream);
+}
+
 int dualkv_check_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DUALKV_ERR_CUDA;
   int dev = 0;
@@ -492,6 +558,7 @@ void dualkv_release(void) {
   for (cudaEvent_t e : g_event_pool) cudaEventDestroy(e);
   g_event_pool.clear();
   g_plans.clear();
+  g_offsets.clear();
   for (auto& kv : g_status) cudaFree(kv.second);
   g_status.clear();
 }

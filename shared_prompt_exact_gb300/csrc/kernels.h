@@ -118,4 +118,12 @@ cudaError_t launch_dq512(const CUtensorMap& tBlk, const CUtensorMap& tK, const D
 // One CTA waits on an mbarrier that nothing completes, with a bounded wait of limit_ns.
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, uint32_t* status, cudaStream_t st);
 
+// ---- per-token tensors between the replicated and the packed layout (pack.cu)
+// kind 0 = pack (replicated -> packed), 1 = unpack (packed -> replicated),
+// 2 = fold (replicated -> packed, prompt rows summed over the replicas).
+// Rows are row_elems bf16 (a multiple of 8); d_off is R_offsets in device memory.
+int pack_group_lanes(int row_elems);
+cudaError_t launch_pack(int kind, const void* src, void* dst, const int32_t* d_off, int P, int N, int64_t T,
+                        int row_elems, int num_sms, cudaStream_t st);
+
 }  // namespace dkv

@@ -30,9 +30,10 @@ DUALKV_ERR_UNSUPPORTED = 6
 # every symbol the header declares
 EXPORTS = ("dualkv_fwd", "dualkv_bwd_workspace_bytes", "dualkv_bwd", "dualkv_build_index", "dualkv_rho",
            "dualkv_pairs", "dualkv_check_status", "dualkv_error_string", "dualkv_profile_enable",
-           "dualkv_profile_read", "dualkv_selftest_timeout", "dualkv_bwd_noalloc", "dualkv_release")
+           "dualkv_profile_read", "dualkv_selftest_timeout", "dualkv_bwd_noalloc", "dualkv_release",
+           "dualkv_pack", "dualkv_unpack", "dualkv_fold")
 NOALLOC_SCRATCH_BYTES = 32 << 20
-KERNEL_KINDS = ("fwd", "prep", "dkv", "reduce", "dq")
+KERNEL_KINDS = ("fwd", "prep", "dkv", "reduce", "dq", "pack")
 
 _lock = threading.Lock()
 _lib = None
@@ -81,6 +82,9 @@ def load(path: Optional[str] = None):
         lib.dualkv_bwd_noalloc.restype = ci
         lib.dualkv_selftest_timeout.argtypes = [ctypes.c_uint64, vp]
         lib.dualkv_selftest_timeout.restype = ci
+        for name in ("dualkv_pack", "dualkv_unpack", "dualkv_fold"):
+            getattr(lib, name).argtypes = [vp, vp, ci, ci, i32p, ci, vp]
+            getattr(lib, name).restype = ci
         lib.dualkv_release.argtypes = []
         lib.dualkv_release.restype = None
         _lib = lib
@@ -167,6 +171,39 @@ def dualkv_bwd_noalloc(q, k, v, out, lse, dout, P, N, R_offsets, Hq, Hkv, D, sca
                                    _offsets(R_offsets), int(Hq), int(Hkv), int(D), float(scale), int(window),
                                    _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream))
     _raise(rc, "dualkv_bwd_noalloc")
+
+
+def _pack_call(fn, name, src, dst, P, N, R_offsets, stream):
+    for nm, t in (("src", src), ("dst", dst)):
+        _check_dev(nm, t, torch.bfloat16)
+        if t.dim() < 2:
+            raise ValueError(f"{name}: {nm} must have a row dimension and at least one more")
+    T = int(P) + int(R_offsets[N])
+    T_rep = int(N) * int(P) + int(R_offsets[N])
+    rows_src, rows_dst = (T, T_rep) if name == "dualkv_unpack" else (T_rep, T)
+    if src.shape[0] != rows_src or dst.shape[0] != rows_dst:
+        raise ValueError(f"{name}: expected {rows_src} source and {rows_dst} destination rows, "
+                         f"got {src.shape[0]} and {dst.shape[0]}")
+    row_elems = src.numel() // rows_src
+    if dst.numel() // rows_dst != row_elems:
+        raise ValueError(f"{name}: src and dst rows must have the same number of elements")
+    rc = fn(_ptr(src), _ptr(dst), int(P), int(N), _offsets(R_offsets), int(row_elems), _stream(stream))
+    _raise(rc, name)
+
+
+def dualkv_pack(x_rep, x_packed, P, N, R_offsets, stream=None) -> None:
+    """x_rep [N*P + R_offsets[N], ...] -> x_packed [P + R_offsets[N], ...] (prompt rows from replica 0)."""
+    _pack_call(load().dualkv_pack, "dualkv_pack", x_rep, x_packed, P, N, R_offsets, stream)
+
+
+def dualkv_unpack(x_packed, x_rep, P, N, R_offsets, stream=None) -> None:
+    """x_packed [T, ...] -> x_rep [T_rep, ...] (prompt rows copied into every replica)."""
+    _pack_call(load().dualkv_unpack, "dualkv_unpack", x_packed, x_rep, P, N, R_offsets, stream)
+
+
+def dualkv_fold(g_rep, g_packed, P, N, R_offsets, stream=None) -> None:
+    """g_rep [T_rep, ...] -> g_packed [T, ...]: prompt rows summed over the N replicas (fp32, in order)."""
+    _pack_call(load().dualkv_fold, "dualkv_fold", g_rep, g_packed, P, N, R_offsets, stream)
 
 
 def dualkv_build_index(P, N, R_offsets):
