@@ -394,6 +394,27 @@ def run_dualkv(args, w):
                     "avg_launch_ms": avg_ms, "algorithmic_flops_per_launch": per_launch_flops}
     kernels = {kk: {"ms_per_launch": (ms / n if n else None), "launches": n} for kk, (ms, n) in kt.items()}
 
+    # the same step as W head-range calls of Hkv / W kv-heads each (the per-rank
+    # share of a W-way head split), run back to back on this GPU
+    head_groups = {}
+    for W in (2, Hkv):
+        if W < 2 or Hkv % W:
+            continue
+        ranges = [(i * Hkv // W, (i + 1) * Hkv // W) for i in range(W)]
+
+        def hstep(ranges=ranges):
+            for lo, hi in ranges:
+                dualkv.dualkv_fwd_heads(q, k, v, w.P, w.N, w.offsets, Hq, Hkv, D, w.scale, w.window, lo, hi, out,
+                                        lse, stream)
+                dualkv.dualkv_bwd_heads(q, k, v, out, lse, do, w.P, w.N, w.offsets, Hq, Hkv, D, w.scale, w.window,
+                                        lo, hi, dq, dk, dv, ws, None, stream)
+
+        hstep()
+        ms_h = max_over_ranks(timed(hstep, max(1, min(args.steps, 5))), world, dev)
+        head_groups[f"{W}x{Hkv // W}kv"] = {"ms_per_step": ms_h, "tflops": f_step / (ms_h * 1e-3) / 1e12,
+                                             "ms_per_group": ms_h / W}
+    dualkv.dualkv_check_status(stream)
+
     # end to end through the C ABI with host buffers: pinned H2D of the step's
     # inputs, forward + backward, D2H of every output
     e2e = None
@@ -482,6 +503,7 @@ def run_dualkv(args, w):
             "e2e": e2e,
             "replicated": replicated,
             "tensor_packing": packing,
+            "head_groups": head_groups,
             "gpu_launches": int(round(launches_per_step * args.steps)),
             "clocks": clocks,
         }

@@ -106,6 +106,31 @@ int dualkv_bwd(const void* q, const void* k, const void* v, const void* out, con
                void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Head-range variants (paper abstract: the kernels integrate with Ulysses
+ * sequence parallelism, which hands each rank a group of heads after its
+ * all-to-all; heads never interact inside attention).  Same arguments, layout
+ * and results as dualkv_fwd / dualkv_bwd on the full-head tensors, but only
+ * kv-heads [kv_head_begin, kv_head_end) and their q-heads
+ * [kv_head_begin * G, kv_head_end * G) (G = Hq / Hkv) are computed: out, lse
+ * and dq of those q-heads and dk, dv of those kv-heads are written, every
+ * other head of every output is left untouched, and only those heads of the
+ * inputs are read.  Each head's result is bitwise identical to the one the
+ * full call writes, so disjoint ranges may run as separate calls (one per
+ * stream, or interleaved with the exchange that brings in each group) and
+ * together equal one full call.  Calls on disjoint ranges may overlap on the
+ * GPU if each backward call has its own workspace.  The workspace of
+ * dualkv_bwd_heads needs at most dualkv_bwd_workspace_bytes() of the full
+ * layout.  DUALKV_ERR_INVALID unless 0 <= kv_head_begin < kv_head_end <= Hkv.
+ */
+int dualkv_fwd_heads(const void* q, const void* k, const void* v, int P, int N, const int32_t* R_offsets, int Hq,
+                     int Hkv, int D, float scale, int window, int kv_head_begin, int kv_head_end, void* out,
+                     float* lse, void* stream);
+int dualkv_bwd_heads(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout,
+                     int P, int N, const int32_t* R_offsets, int Hq, int Hkv, int D, float scale, int window,
+                     int kv_head_begin, int kv_head_end, void* dq, void* dk, void* dv, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/*
  * Packing indices (host only, no GPU needed; paper abstract: the pipeline
  * "repacks N(P+R) tokens into P+NR tokens").  All outputs are HOST int32:
  *   seg_id[T]          -1 for prompt rows, else the segment of the row

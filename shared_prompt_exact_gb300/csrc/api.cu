@@ -71,10 +71,11 @@ struct DevOffsets {
 };
 std::map<std::string, std::unique_ptr<DevOffsets>> g_offsets;  // (device, P, N, R_offsets) -> device copy
 
-std::string plan_key(int device, int P, int N, const int32_t* off, int Hq, int Hkv, int D, int window) {
+std::string plan_key(int device, int P, int N, const int32_t* off, int Hq, int Hkv, int D, int window, int kv_lo = 0,
+                     int kv_hi = 0) {
   std::string k;
   k.reserve(64 + 4 * (N + 1));
-  int32_t hdr[7] = {device, P, N, Hq, Hkv, D, window <= 0 ? 0 : window};
+  int32_t hdr[9] = {device, P, N, Hq, Hkv, D, window <= 0 ? 0 : window, kv_lo, kv_hi};
   k.append(reinterpret_cast<const char*>(hdr), sizeof(hdr));
   k.append(reinterpret_cast<const char*>(off), sizeof(int32_t) * (N + 1));
   return k;
@@ -128,18 +129,20 @@ int make_tmap(CUtensorMap* m, const void* base, int64_t T, int H, int D, int box
   return r == CUDA_SUCCESS ? DUALKV_OK : DUALKV_ERR_CUDA;
 }
 
-// Looks up (or builds) the plan of a layout; caller holds g_mu.
-int get_plan(int P, int N, const int32_t* off, int Hq, int Hkv, int D, int window, bool need_bwd, DevPlan** out) {
+// Looks up (or builds) the plan of a layout restricted to kv-heads [kv_lo, kv_hi);
+// caller holds g_mu.
+int get_plan(int P, int N, const int32_t* off, int Hq, int Hkv, int D, int window, int kv_lo, int kv_hi,
+             bool need_bwd, DevPlan** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DUALKV_ERR_CUDA;
-  const std::string key = plan_key(dev, P, N, off, Hq, Hkv, D, window);
+  const std::string key = plan_key(dev, P, N, off, Hq, Hkv, D, window, kv_lo, kv_hi);
   auto& slot = g_plans[key];
   if (!slot) {
     slot.reset(new DevPlan());
     slot->device = dev;
   }
   DevPlan* pl = slot.get();
-  Layout L{P, N, std::vector<int32_t>(off, off + N + 1), Hq, Hkv, D, window <= 0 ? 0 : window};
+  Layout L{P, N, std::vector<int32_t>(off, off + N + 1), Hq, Hkv, D, window <= 0 ? 0 : window, kv_lo, kv_hi};
   if (!pl->fwd_ready) {
     auto items = plan_qtiles(L, fwd_query_tile(D), fwd_key_tile(D));
     if (upload(&pl->fwd_items, items) != cudaSuccess) return DUALKV_ERR_CUDA;
@@ -288,13 +291,10 @@ int pack_call(int kind, const void* src, void* dst, int P, int N, const int32_t*
 bool supported_d(int D) { return D == 64 || D == 128 || D == 512; }  // backward
 bool supported_fwd_d(int D) { return D == 64 || D == 128 || D == 512; }
 
-}  // namespace
-
-extern "C" {
-
-int dualkv_fwd(const void* q, const void* k, const void* v, int P, int N, const int32_t* R_offsets, int Hq, int Hkv,
-               int D, float scale, int window, void* out, float* lse, void* stream) {
+int fwd_impl(const void* q, const void* k, const void* v, int P, int N, const int32_t* R_offsets, int Hq, int Hkv,
+             int D, float scale, int window, int kv_lo, int kv_hi, void* out, float* lse, void* stream) {
   if (validate_layout(P, N, R_offsets, Hq, Hkv, D)) return DUALKV_ERR_INVALID;
+  if (kv_lo < 0 || kv_hi > Hkv || kv_lo >= kv_hi) return DUALKV_ERR_INVALID;
   if (!(scale > 0.f) || !std::isfinite(scale)) return DUALKV_ERR_INVALID;
   if (!q || !k || !v || !out || !lse) return DUALKV_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse)) return DUALKV_ERR_ALIGN;
@@ -304,7 +304,7 @@ int dualkv_fwd(const void* q, const void* k, const void* v, int P, int N, const 
   int rc = ensure_encode();
   if (rc) return rc;
   DevPlan* pl = nullptr;
-  if ((rc = get_plan(P, N, R_offsets, Hq, Hkv, D, window, false, &pl))) return rc;
+  if ((rc = get_plan(P, N, R_offsets, Hq, Hkv, D, window, kv_lo, kv_hi, false, &pl))) return rc;
   uint32_t* status = nullptr;
   if ((rc = status_word(pl->device, &status))) return rc;
   CUtensorMap tq, tk, tv;
@@ -319,21 +319,11 @@ int dualkv_fwd(const void* q, const void* k, const void* v, int P, int N, const 
   return DUALKV_OK;
 }
 
-size_t dualkv_bwd_workspace_bytes(int P, int N, const int32_t* R_offsets, int Hq, int Hkv, int D, int window) {
-  if (validate_layout(P, N, R_offsets, Hq, Hkv, D) || !supported_d(D)) return 0;
-  Layout L{P, N, std::vector<int32_t>(R_offsets, R_offsets + N + 1), Hq, Hkv, D, window <= 0 ? 0 : window};
-  if (D == 512) {
-    Plan512 p5 = plan_512(L, plan_qtiles(L, 128, 128), kMaxDkvIters);
-    return ws_layout(L.T(), Hq, D, p5.nslots, p5.n_blocks).total;
-  }
-  KVPlan kv = plan_kvtiles(L, dkv_key_tile(D), dkv_query_block(D), kMaxDkvIters);
-  return ws_layout(L.T(), Hq, D, kv.nslots, 0).total;
-}
-
-int dualkv_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout, int P,
-               int N, const int32_t* R_offsets, int Hq, int Hkv, int D, float scale, int window, void* dq, void* dk,
-               void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+int bwd_impl(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout, int P,
+             int N, const int32_t* R_offsets, int Hq, int Hkv, int D, float scale, int window, int kv_lo, int kv_hi,
+             void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
   if (validate_layout(P, N, R_offsets, Hq, Hkv, D)) return DUALKV_ERR_INVALID;
+  if (kv_lo < 0 || kv_hi > Hkv || kv_lo >= kv_hi) return DUALKV_ERR_INVALID;
   if (!(scale > 0.f) || !std::isfinite(scale)) return DUALKV_ERR_INVALID;
   if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return DUALKV_ERR_INVALID;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) || !aligned16(dout) ||
@@ -347,7 +337,7 @@ int dualkv_bwd(const void* q, const void* k, const void* v, const void* out, con
   int rc = ensure_encode();
   if (rc) return rc;
   DevPlan* pl = nullptr;
-  if ((rc = get_plan(P, N, R_offsets, Hq, Hkv, D, window, true, &pl))) return rc;
+  if ((rc = get_plan(P, N, R_offsets, Hq, Hkv, D, window, kv_lo, kv_hi, true, &pl))) return rc;
   const WsLayout ws = ws_layout(T, Hq, D, pl->nslots, D == 512 ? pl->n_blocks : 0);
   if (workspace_bytes < ws.total) return DUALKV_ERR_WORKSPACE;
   uint32_t* status = nullptr;
@@ -359,7 +349,9 @@ int dualkv_bwd(const void* q, const void* k, const void* v, const void* out, con
   const int W = window <= 0 ? 0 : window;
   const float sl2 = scale * 1.4426950408889634f;
 
-  PrepArgs pa{static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, delta, lse2, T, Hq, D};
+  const int gs = Hq / Hkv;
+  PrepArgs pa{static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, delta, lse2, T, Hq, D,
+              kv_lo * gs, kv_hi * gs};
   if (timed(DUALKV_KERNEL_PREP, st, [&] { return launch_prep(pa, st); }) != cudaSuccess) return DUALKV_ERR_CUDA;
 
   if (D == 512) {
@@ -419,6 +411,49 @@ int dualkv_bwd(const void* q, const void* k, const void* v, const void* out, con
     return DUALKV_ERR_CUDA;
   return DUALKV_OK;
 }
+
+}  // namespace
+
+extern "C" {
+
+int dualkv_fwd(const void* q, const void* k, const void* v, int P, int N, const int32_t* R_offsets, int Hq, int Hkv,
+               int D, float scale, int window, void* out, float* lse, void* stream) {
+  return fwd_impl(q, k, v, P, N, R_offsets, Hq, Hkv, D, scale, window, 0, Hkv, out, lse, stream);
+}
+
+int dualkv_fwd_heads(const void* q, const void* k, const void* v, int P, int N, const int32_t* R_offsets, int Hq,
+                     int Hkv, int D, float scale, int window, int kv_head_begin, int kv_head_end, void* out,
+                     float* lse, void* stream) {
+  return fwd_impl(q, k, v, P, N, R_offsets, Hq, Hkv, D, scale, window, kv_head_begin, kv_head_end, out, lse, stream);
+}
+
+
+size_t dualkv_bwd_workspace_bytes(int P, int N, const int32_t* R_offsets, int Hq, int Hkv, int D, int window) {
+  if (validate_layout(P, N, R_offsets, Hq, Hkv, D) || !supported_d(D)) return 0;
+  Layout L{P, N, std::vector<int32_t>(R_offsets, R_offsets + N + 1), Hq, Hkv, D, window <= 0 ? 0 : window};
+  if (D == 512) {
+    Plan512 p5 = plan_512(L, plan_qtiles(L, 128, 128), kMaxDkvIters);
+    return ws_layout(L.T(), Hq, D, p5.nslots, p5.n_blocks).total;
+  }
+  KVPlan kv = plan_kvtiles(L, dkv_key_tile(D), dkv_query_block(D), kMaxDkvIters);
+  return ws_layout(L.T(), Hq, D, kv.nslots, 0).total;
+}
+
+int dualkv_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout, int P,
+               int N, const int32_t* R_offsets, int Hq, int Hkv, int D, float scale, int window, void* dq, void* dk,
+               void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, out, lse, dout, P, N, R_offsets, Hq, Hkv, D, scale, window, 0, Hkv, dq, dk, dv, workspace,
+                  workspace_bytes, stream);
+}
+
+int dualkv_bwd_heads(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout,
+                     int P, int N, const int32_t* R_offsets, int Hq, int Hkv, int D, float scale, int window,
+                     int kv_head_begin, int kv_head_end, void* dq, void* dk, void* dv, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  return bwd_impl(q, k, v, out, lse, dout, P, N, R_offsets, Hq, Hkv, D, scale, window, kv_head_begin, kv_head_end,
+                  dq, dk, dv, workspace, workspace_bytes, stream);
+}
+
 
 int dualkv_build_index(int P, int N, const int32_t* R_offsets, int32_t* seg_id, int32_t* pos_id,
                        int32_t* cu_seqlens_rep, int32_t* rep2pack) {

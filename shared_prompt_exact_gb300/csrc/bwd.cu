@@ -34,14 +34,18 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepArgs a) {
   constexpr int LPR = (D / 8) < 32 ? (D / 8) : 32;  // lanes per row
   constexpr int PASSES = D / (8 * LPR);
   constexpr int RPW = 32 / LPR;                       // rows per warp
-  const int64_t nrows = a.T * a.Hq;
+  const int h_hi = a.h_hi < 0 ? a.Hq : a.h_hi;
+  const int nh = h_hi - a.h_lo;
+  const int64_t nrows = a.T * nh;
   const int64_t warp_global = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x / 32);
   const int sub = (threadIdx.x & 31) / LPR, l = (threadIdx.x & 31) % LPR;
-  const int64_t r = warp_global * RPW + sub;  // row = t * Hq + h
+  const int64_t r = warp_global * RPW + sub;  // row = t * nh + (h - h_lo)
+  const int64_t t = r / nh;
+  const int h = a.h_lo + (int)(r % nh);
   float acc = 0.f;
   if (r < nrows) {
-    const uint4* po = reinterpret_cast<const uint4*>(a.out + r * D);
-    const uint4* pd = reinterpret_cast<const uint4*>(a.dout + r * D);
+    const uint4* po = reinterpret_cast<const uint4*>(a.out + (t * a.Hq + h) * D);
+    const uint4* pd = reinterpret_cast<const uint4*>(a.dout + (t * a.Hq + h) * D);
 #pragma unroll
     for (int p = 0; p < PASSES; ++p) {
       const uint4 o = po[p * LPR + l], g = pd[p * LPR + l];
@@ -58,8 +62,6 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepArgs a) {
 #pragma unroll
   for (int s = LPR / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
   if (r < nrows && l == 0) {
-    const int64_t t = r / a.Hq;
-    const int h = (int)(r % a.Hq);
     a.delta[(int64_t)h * a.T + t] = acc;
     a.lse2[(int64_t)h * a.T + t] = a.lse[(int64_t)h * a.T + t] * kLog2e;
   }
@@ -748,7 +750,7 @@ int dkv_key_tile(int /*D*/) { return 128; }
 int dkv_query_block(int /*D*/) { return 64; }
 
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st) {
-  const int64_t nrows = a.T * a.Hq;
+  const int64_t nrows = a.T * ((a.h_hi < 0 ? a.Hq : a.h_hi) - a.h_lo);
   auto grid_for = [&](int lpr) {
     const int64_t rows_per_block = (256 / 32) * (32 / lpr);
     return (unsigned)((nrows + rows_per_block - 1) / rows_per_block);

@@ -32,6 +32,7 @@ struct PrepArgs {
   float* lse2;   // [Hq, T], lse * log2(e)
   int64_t T;
   int Hq, D;
+  int h_lo = 0, h_hi = -1;  // q-heads [h_lo, h_hi) are prepared (h_hi < 0: all)
 };
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st);
 

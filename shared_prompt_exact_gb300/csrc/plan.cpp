@@ -88,7 +88,8 @@ std::vector<QTileItem> plan_qtiles(const Layout& L, int tile_rows, int key_tile)
         it.reg[1] = KeyRegion{q.row0, q.pos0, 0, 0, 0};  // prompt queries: one region
       else
         it.reg[1] = clip_keys(q, p_first, p_last, L.window, key_tile);
-      for (int h = 0; h < L.Hq; ++h) {
+      const int gs = L.Hq / L.Hkv;
+      for (int h = L.kv_begin() * gs; h < L.kv_end() * gs; ++h) {
         it.head = h;
         items.push_back(it);
       }
@@ -142,7 +143,7 @@ KVPlan plan_kvtiles(const Layout& L, int key_tile, int q_block, int max_iters) {
   }
   // Chunks are emitted split-major (chunk s of every key tile of a kv-head, then
   // chunk s+1): CTAs that run together then stream the same query blocks.
-  for (int g = 0; g < L.Hkv; ++g) {
+  for (int g = L.kv_begin(); g < L.kv_end(); ++g) {
     std::vector<std::vector<KVTileItem>> per_tile;
     int max_split = 0;
     for (const TileList& tl : tiles) {
@@ -233,7 +234,7 @@ Plan512 plan_512(const Layout& L, const std::vector<QTileItem>& qitems, int max_
     const int R = L.off[n + 1] - L.off[n];
     for (int t = 0; t * kTile < R; ++t) ktile[seg_tile_base[n] + t] = {L.P + L.off[n] + t * kTile, std::min(kTile, R - t * kTile)};
   }
-  for (int g = 0; g < L.Hkv; ++g)
+  for (int g = L.kv_begin(); g < L.kv_end(); ++g)
     for (int kt = 0; kt < ntiles; ++kt) {
       const auto& lst = lists[(size_t)kt * L.Hkv + g];
       const int begin = (int)pl.entries.size();

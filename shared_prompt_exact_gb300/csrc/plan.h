@@ -55,7 +55,11 @@ struct Layout {
   int P, N;
   std::vector<int32_t> off;  // N+1
   int Hq, Hkv, D, window;
+  // kv-heads [kv_lo, kv_hi) and their q-head groups get work items (kv_hi < 0: all)
+  int kv_lo = 0, kv_hi = -1;
   int64_t T() const { return (int64_t)P + off[N]; }
+  int kv_begin() const { return kv_lo; }
+  int kv_end() const { return kv_hi < 0 ? Hkv : kv_hi; }
 };
 
 // Returns an error string, or nullptr when the layout is valid.

@@ -31,7 +31,7 @@ DUALKV_ERR_UNSUPPORTED = 6
 EXPORTS = ("dualkv_fwd", "dualkv_bwd_workspace_bytes", "dualkv_bwd", "dualkv_build_index", "dualkv_rho",
            "dualkv_pairs", "dualkv_check_status", "dualkv_error_string", "dualkv_profile_enable",
            "dualkv_profile_read", "dualkv_selftest_timeout", "dualkv_bwd_noalloc", "dualkv_release",
-           "dualkv_pack", "dualkv_unpack", "dualkv_fold")
+           "dualkv_pack", "dualkv_unpack", "dualkv_fold", "dualkv_fwd_heads", "dualkv_bwd_heads")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 KERNEL_KINDS = ("fwd", "prep", "dkv", "reduce", "dq", "pack")
 
@@ -64,6 +64,11 @@ def load(path: Optional[str] = None):
         lib.dualkv_bwd.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, i32p, ci, ci, ci, cf, ci, vp, vp, vp, vp,
                                    ctypes.c_size_t, vp]
         lib.dualkv_bwd.restype = ci
+        lib.dualkv_fwd_heads.argtypes = [vp, vp, vp, ci, ci, i32p, ci, ci, ci, cf, ci, ci, ci, vp, vp, vp]
+        lib.dualkv_fwd_heads.restype = ci
+        lib.dualkv_bwd_heads.argtypes = [vp, vp, vp, vp, vp, vp, ci, ci, i32p, ci, ci, ci, cf, ci, ci, ci, vp, vp,
+                                         vp, vp, ctypes.c_size_t, vp]
+        lib.dualkv_bwd_heads.restype = ci
         lib.dualkv_build_index.argtypes = [ci, ci, i32p, i32p, i32p, i32p, i32p]
         lib.dualkv_build_index.restype = ci
         lib.dualkv_rho.argtypes = [ci, ci, i32p]
@@ -155,6 +160,34 @@ def dualkv_bwd(q, k, v, out, lse, dout, P, N, R_offsets, Hq, Hkv, D, scale, wind
                            _offsets(R_offsets), int(Hq), int(Hkv), int(D), float(scale), int(window), _ptr(dq),
                            _ptr(dk), _ptr(dv), _ptr(workspace), int(workspace_bytes), _stream(stream))
     _raise(rc, "dualkv_bwd")
+
+
+def dualkv_fwd_heads(q, k, v, P, N, R_offsets, Hq, Hkv, D, scale, window, kv_head_begin, kv_head_end, out, lse,
+                     stream=None) -> None:
+    """dualkv_fwd restricted to kv-heads [kv_head_begin, kv_head_end) and their q-heads."""
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
+                        ("out", out, torch.bfloat16), ("lse", lse, torch.float32)):
+        _check_dev(name, t, dt)
+    rc = load().dualkv_fwd_heads(_ptr(q), _ptr(k), _ptr(v), int(P), int(N), _offsets(R_offsets), int(Hq), int(Hkv),
+                                 int(D), float(scale), int(window), int(kv_head_begin), int(kv_head_end), _ptr(out),
+                                 _ptr(lse), _stream(stream))
+    _raise(rc, "dualkv_fwd_heads")
+
+
+def dualkv_bwd_heads(q, k, v, out, lse, dout, P, N, R_offsets, Hq, Hkv, D, scale, window, kv_head_begin,
+                     kv_head_end, dq, dk, dv, workspace, workspace_bytes=None, stream=None) -> None:
+    """dualkv_bwd restricted to kv-heads [kv_head_begin, kv_head_end) and their q-heads."""
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
+                        ("out", out, torch.bfloat16), ("lse", lse, torch.float32), ("dout", dout, torch.bfloat16),
+                        ("dq", dq, torch.bfloat16), ("dk", dk, torch.bfloat16), ("dv", dv, torch.bfloat16)):
+        _check_dev(name, t, dt)
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = load().dualkv_bwd_heads(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout), int(P), int(N),
+                                 _offsets(R_offsets), int(Hq), int(Hkv), int(D), float(scale), int(window),
+                                 int(kv_head_begin), int(kv_head_end), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                                 int(workspace_bytes), _stream(stream))
+    _raise(rc, "dualkv_bwd_heads")
 
 
 def dualkv_bwd_noalloc(q, k, v, out, lse, dout, P, N, R_offsets, Hq, Hkv, D, scale, window, dq, dk, dv,
