@@ -514,6 +514,98 @@ def run_dualkv(args, w):
     return 0
 
 
+# ------------------------------------------------------------------ layer stacks
+def run_layers(args, w):
+    """A stack of attention layers over one packed micro-batch: `--layers` is a
+    pattern of S (sliding window `--slide-window`) and G (global) layers.  One
+    step = dualkv_fwd_layers over the stack + dualkv_bwd_layers in reverse layer
+    order; the metric is the stack's useful TFLOP/s."""
+    from shared_prompt_exact_gb300 import build as pbuild
+    from shared_prompt_exact_gb300 import dualkv
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pbuild.build()
+    dualkv.load()
+    windows = [args.slide_window if c == "S" else 0 for c in args.layers]
+    n = len(windows)
+    T, Hq, Hkv, D = w.T, w.Hq, w.Hkv, w.D
+    gen = torch.Generator(device=dev).manual_seed(w.seed)
+    rnd = lambda *shape: torch.randn(*shape, generator=gen, device=dev).to(torch.bfloat16)  # noqa: E731
+    qs = [rnd(T, Hq, D) for _ in range(n)]
+    ks = [rnd(T, Hkv, D) for _ in range(n)]
+    vs = [rnd(T, Hkv, D) for _ in range(n)]
+    dos = [rnd(T, Hq, D) for _ in range(n)]
+    outs = [torch.empty_like(x) for x in qs]
+    lses = [torch.empty(Hq, T, dtype=torch.float32, device=dev) for _ in range(n)]
+    dqs, dks, dvs = ([torch.empty_like(x) for x in xs] for xs in (qs, ks, vs))
+    nbytes = dualkv.dualkv_bwd_layers_workspace_bytes(windows, w.P, w.N, w.offsets, Hq, Hkv, D)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    r = lambda xs: xs[::-1]  # noqa: E731
+
+    def step():
+        dualkv.dualkv_fwd_layers(qs, ks, vs, windows, w.P, w.N, w.offsets, Hq, Hkv, D, w.scale, outs, lses, stream)
+        dualkv.dualkv_bwd_layers(r(qs), r(ks), r(vs), r(outs), r(lses), r(dos), r(windows), w.P, w.N, w.offsets, Hq,
+                                 Hkv, D, w.scale, r(dqs), r(dks), r(dvs), ws, None, stream)
+
+    flops = 0.0
+    per_window = {}
+    for W in windows:
+        pairs = dualkv.dualkv_pairs(w.P, w.N, w.offsets, W)
+        flops += sum(useful_flops(pairs, D, Hq))
+        per_window[str(W)] = pairs
+    for _ in range(max(args.warmup, 1)):
+        step()
+    dualkv.dualkv_check_status(stream)
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_start = time.time()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t_end = time.time()
+    ms, value = aggregate(e0.elapsed_time(e1) / args.steps, flops, world, dev)
+    dualkv.dualkv_profile_read()
+    dualkv.dualkv_profile_enable(True)
+    step()
+    torch.cuda.synchronize(dev)
+    kt = dualkv.dualkv_profile_read()
+    dualkv.dualkv_profile_enable(False)
+    dualkv.dualkv_check_status(stream)
+    sampler.stop()
+    pk = peaks()
+    if rank == 0:
+        line = {
+            "metric": "DualKV layer stack fwd+bwd useful TFLOP/s", "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{w.name}-stack-{args.layers}", "layers": args.layers, "windows": windows,
+                       "P": w.P, "N": w.N, "R": list(sorted(set(w.R))), "Hq": Hq, "Hkv": Hkv, "D": D,
+                       "pairs_per_head": per_window,
+                       "l2": "no flush: every layer's inputs are larger than L2"},
+            "pct_bf16_peak": {"measured_sustained": value / world / pk["bf16_sustained"]},
+            "kernels": {kk: {"ms_per_launch": (t / c if c else None), "launches": c} for kk, (t, c) in kt.items()},
+            "gpu_launches": int(sum(c for _, c in kt.values()) * args.steps),
+            "clocks": sampler.summary(t_start, t_end),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -528,11 +620,21 @@ def main(argv=None):
     ap.add_argument("--no-replicated", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pack", action="store_true", help="skip the pack/unpack/fold measurement")
+    ap.add_argument("--layers", default=None,
+                    help="time a layer stack instead: a pattern of S (sliding) and G (global) layers, e.g. SSSSSG")
+    ap.add_argument("--slide-window", type=int, default=1024, help="window of the S layers of --layers")
     args = ap.parse_args(argv)
     w = wl.WORKLOADS[args.config]
     if args.heads:
         hq, hkv = (int(x) for x in args.heads.split(","))
         w = dataclasses.replace(w, name=f"{w.name}-h{hq}x{hkv}", Hq=hq, Hkv=hkv)
+    if args.layers:
+        if set(args.layers) - {"S", "G"}:
+            ap.error("--layers takes a pattern of S and G")
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "--layers times the GPU path only"}))
+            return 0
+        return run_layers(args, w)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_dualkv(args, w)

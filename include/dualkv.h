@@ -131,6 +131,32 @@ int dualkv_bwd_heads(const void* q, const void* k, const void* v, const void* ou
                      size_t workspace_bytes, void* stream);
 
 /*
+ * Layer stacks (paper abstract: the method extends to models that interleave
+ * sliding-window and global attention layers, with head dimension 512).  A
+ * stack of n_layers attention layers over one packed micro-batch: every layer
+ * shares the layout (P, N, R_offsets, Hq, Hkv, D, scale) and has its own
+ * tensors and its own window (window[l] <= 0: global causal).  The layers run
+ * back to back on `stream` in the order given (pass them in reverse order to
+ * dualkv_bwd_layers for a model's backward pass); the plan of each distinct
+ * window is built once and reused by every layer that has it, and the
+ * backward layers share one workspace of at least
+ * dualkv_bwd_layers_workspace_bytes() (the largest that any of its windows
+ * needs; 0 for invalid input).  q[l], k[l], ... are host arrays of n_layers
+ * device pointers, window a host array of n_layers ints.  The results are
+ * bitwise those of n_layers dualkv_fwd / dualkv_bwd calls.  Every pointer of
+ * every layer is checked before the first layer is launched.
+ */
+size_t dualkv_bwd_layers_workspace_bytes(int n_layers, const int32_t* window, int P, int N, const int32_t* R_offsets,
+                                         int Hq, int Hkv, int D);
+int dualkv_fwd_layers(int n_layers, const void* const* q, const void* const* k, const void* const* v,
+                      const int32_t* window, int P, int N, const int32_t* R_offsets, int Hq, int Hkv, int D,
+                      float scale, void* const* out, float* const* lse, void* stream);
+int dualkv_bwd_layers(int n_layers, const void* const* q, const void* const* k, const void* const* v,
+                      const void* const* out, const float* const* lse, const void* const* dout, const int32_t* window,
+                      int P, int N, const int32_t* R_offsets, int Hq, int Hkv, int D, float scale, void* const* dq,
+                      void* const* dk, void* const* dv, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Packing indices (host only, no GPU needed; paper abstract: the pipeline
  * "repacks N(P+R) tokens into P+NR tokens").  All outputs are HOST int32:
  *   seg_id[T]          -1 for prompt rows, else the segment of the row

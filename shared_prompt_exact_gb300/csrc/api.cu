@@ -455,6 +455,62 @@ int dualkv_bwd_heads(const void* q, const void* k, const void* v, const void* ou
 }
 
 
+size_t dualkv_bwd_layers_workspace_bytes(int n_layers, const int32_t* window, int P, int N, const int32_t* R_offsets,
+                                         int Hq, int Hkv, int D) {
+  if (n_layers < 1 || !window) return 0;
+  size_t need = 0;
+  for (int l = 0; l < n_layers; ++l) {
+    const size_t b = dualkv_bwd_workspace_bytes(P, N, R_offsets, Hq, Hkv, D, window[l]);
+    if (b == 0) return 0;
+    need = b > need ? b : need;
+  }
+  return need;
+}
+
+int dualkv_fwd_layers(int n_layers, const void* const* q, const void* const* k, const void* const* v,
+                      const int32_t* window, int P, int N, const int32_t* R_offsets, int Hq, int Hkv, int D,
+                      float scale, void* const* out, float* const* lse, void* stream) {
+  if (n_layers < 1 || !q || !k || !v || !window || !out || !lse) return DUALKV_ERR_INVALID;
+  if (validate_layout(P, N, R_offsets, Hq, Hkv, D) || !supported_fwd_d(D)) return DUALKV_ERR_INVALID;
+  // check every layer before the first launch
+  for (int l = 0; l < n_layers; ++l) {
+    if (!q[l] || !k[l] || !v[l] || !out[l] || !lse[l]) return DUALKV_ERR_INVALID;
+    if (!aligned16(q[l]) || !aligned16(k[l]) || !aligned16(v[l]) || !aligned16(out[l]) || !aligned16(lse[l]))
+      return DUALKV_ERR_ALIGN;
+  }
+  for (int l = 0; l < n_layers; ++l) {
+    const int rc = fwd_impl(q[l], k[l], v[l], P, N, R_offsets, Hq, Hkv, D, scale, window[l], 0, Hkv, out[l], lse[l],
+                            stream);
+    if (rc) return rc;
+  }
+  return DUALKV_OK;
+}
+
+int dualkv_bwd_layers(int n_layers, const void* const* q, const void* const* k, const void* const* v,
+                      const void* const* out, const float* const* lse, const void* const* dout, const int32_t* window,
+                      int P, int N, const int32_t* R_offsets, int Hq, int Hkv, int D, float scale, void* const* dq,
+                      void* const* dk, void* const* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  if (n_layers < 1 || !q || !k || !v || !out || !lse || !dout || !window || !dq || !dk || !dv)
+    return DUALKV_ERR_INVALID;
+  if (validate_layout(P, N, R_offsets, Hq, Hkv, D) || !supported_d(D)) return DUALKV_ERR_INVALID;
+  for (int l = 0; l < n_layers; ++l) {
+    const void* ptrs[9] = {q[l], k[l], v[l], out[l], lse[l], dout[l], dq[l], dk[l], dv[l]};
+    for (const void* p : ptrs) {
+      if (!p) return DUALKV_ERR_INVALID;
+      if (!aligned16(p)) return DUALKV_ERR_ALIGN;
+    }
+  }
+  const size_t need = dualkv_bwd_layers_workspace_bytes(n_layers, window, P, N, R_offsets, Hq, Hkv, D);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || need == 0 || workspace_bytes < need)
+    return DUALKV_ERR_WORKSPACE;
+  for (int l = 0; l < n_layers; ++l) {
+    const int rc = bwd_impl(q[l], k[l], v[l], out[l], lse[l], dout[l], P, N, R_offsets, Hq, Hkv, D, scale, window[l],
+                            0, Hkv, dq[l], dk[l], dv[l], workspace, workspace_bytes, stream);
+    if (rc) return rc;
+  }
+  return DUALKV_OK;
+}
+
 int dualkv_build_index(int P, int N, const int32_t* R_offsets, int32_t* seg_id, int32_t* pos_id,
                        int32_t* cu_seqlens_rep, int32_t* rep2pack) {
   if (P < 0 || N < 1 || !R_offsets || R_offsets[0] != 0) return DUALKV_ERR_INVALID;

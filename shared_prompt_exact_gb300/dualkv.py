@@ -31,7 +31,8 @@ DUALKV_ERR_UNSUPPORTED = 6
 EXPORTS = ("dualkv_fwd", "dualkv_bwd_workspace_bytes", "dualkv_bwd", "dualkv_build_index", "dualkv_rho",
            "dualkv_pairs", "dualkv_check_status", "dualkv_error_string", "dualkv_profile_enable",
            "dualkv_profile_read", "dualkv_selftest_timeout", "dualkv_bwd_noalloc", "dualkv_release",
-           "dualkv_pack", "dualkv_unpack", "dualkv_fold", "dualkv_fwd_heads", "dualkv_bwd_heads")
+           "dualkv_pack", "dualkv_unpack", "dualkv_fold", "dualkv_fwd_heads", "dualkv_bwd_heads",
+           "dualkv_fwd_layers", "dualkv_bwd_layers", "dualkv_bwd_layers_workspace_bytes")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 KERNEL_KINDS = ("fwd", "prep", "dkv", "reduce", "dq", "pack")
 
@@ -90,6 +91,13 @@ def load(path: Optional[str] = None):
         for name in ("dualkv_pack", "dualkv_unpack", "dualkv_fold"):
             getattr(lib, name).argtypes = [vp, vp, ci, ci, i32p, ci, vp]
             getattr(lib, name).restype = ci
+        lib.dualkv_bwd_layers_workspace_bytes.argtypes = [ci, i32p, ci, ci, i32p, ci, ci, ci]
+        lib.dualkv_bwd_layers_workspace_bytes.restype = ctypes.c_size_t
+        lib.dualkv_fwd_layers.argtypes = [ci, vp, vp, vp, i32p, ci, ci, i32p, ci, ci, ci, cf, vp, vp, vp]
+        lib.dualkv_fwd_layers.restype = ci
+        lib.dualkv_bwd_layers.argtypes = [ci, vp, vp, vp, vp, vp, vp, i32p, ci, ci, i32p, ci, ci, ci, cf, vp, vp, vp,
+                                          vp, ctypes.c_size_t, vp]
+        lib.dualkv_bwd_layers.restype = ci
         lib.dualkv_release.argtypes = []
         lib.dualkv_release.restype = None
         _lib = lib
@@ -188,6 +196,49 @@ def dualkv_bwd_heads(q, k, v, out, lse, dout, P, N, R_offsets, Hq, Hkv, D, scale
                                  int(kv_head_begin), int(kv_head_end), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
                                  int(workspace_bytes), _stream(stream))
     _raise(rc, "dualkv_bwd_heads")
+
+
+def _ptr_array(name, tensors, n, dtype):
+    if len(tensors) != n:
+        raise ValueError(f"{name}: expected {n} tensors, got {len(tensors)}")
+    for i, t in enumerate(tensors):
+        _check_dev(f"{name}[{i}]", t, dtype)
+    return (ctypes.c_void_p * n)(*[t.data_ptr() for t in tensors])
+
+
+def dualkv_bwd_layers_workspace_bytes(windows, P, N, R_offsets, Hq, Hkv, D) -> int:
+    n = len(windows)
+    return int(load().dualkv_bwd_layers_workspace_bytes(n, (ctypes.c_int32 * n)(*[int(x) for x in windows]), int(P),
+                                                         int(N), _offsets(R_offsets), int(Hq), int(Hkv), int(D)))
+
+
+def dualkv_fwd_layers(qs, ks, vs, windows, P, N, R_offsets, Hq, Hkv, D, scale, outs, lses, stream=None) -> None:
+    """Forward of a layer stack: layer l uses qs[l], ks[l], vs[l] and windows[l]."""
+    n = len(windows)
+    bf = torch.bfloat16
+    rc = load().dualkv_fwd_layers(n, _ptr_array("q", qs, n, bf), _ptr_array("k", ks, n, bf), _ptr_array("v", vs, n, bf),
+                                  (ctypes.c_int32 * n)(*[int(x) for x in windows]), int(P), int(N),
+                                  _offsets(R_offsets), int(Hq), int(Hkv), int(D), float(scale),
+                                  _ptr_array("out", outs, n, bf), _ptr_array("lse", lses, n, torch.float32),
+                                  _stream(stream))
+    _raise(rc, "dualkv_fwd_layers")
+
+
+def dualkv_bwd_layers(qs, ks, vs, outs, lses, douts, windows, P, N, R_offsets, Hq, Hkv, D, scale, dqs, dks, dvs,
+                      workspace, workspace_bytes=None, stream=None) -> None:
+    """Backward of a layer stack, layers in the order given, one shared workspace."""
+    n = len(windows)
+    bf = torch.bfloat16
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    rc = load().dualkv_bwd_layers(n, _ptr_array("q", qs, n, bf), _ptr_array("k", ks, n, bf), _ptr_array("v", vs, n, bf),
+                                  _ptr_array("out", outs, n, bf), _ptr_array("lse", lses, n, torch.float32),
+                                  _ptr_array("dout", douts, n, bf), (ctypes.c_int32 * n)(*[int(x) for x in windows]),
+                                  int(P), int(N), _offsets(R_offsets), int(Hq), int(Hkv), int(D), float(scale),
+                                  _ptr_array("dq", dqs, n, bf), _ptr_array("dk", dks, n, bf),
+                                  _ptr_array("dv", dvs, n, bf), _ptr(workspace), int(workspace_bytes),
+                                  _stream(stream))
+    _raise(rc, "dualkv_bwd_layers")
 
 
 def dualkv_bwd_noalloc(q, k, v, out, lse, dout, P, N, R_offsets, Hq, Hkv, D, scale, window, dq, dk, dv,
