@@ -413,11 +413,14 @@ struct DkvCfg {
   static constexpr uint32_t TM_ST = 0, TM_DPT = 2 * BQ, TM_DV = 4 * BQ, TM_DK = 4 * BQ + D, TM_COLS = 512;
 };
 
+// dK/dV uses one more warp than the dQ kernel: warp 10 issues the second GEMM pair.
+constexpr int kDkvThreads = kBwdThreads + 32;
+
 struct DkvSmemCtl {
   uint64_t kv_full;
   uint64_t ring_full[8], ring_empty[8];
-  uint64_t st_full[2], pt_full[2];
-  uint64_t acc_done, drain;
+  uint64_t s_full[2], dp_full[2], p_full[2], ds_full[2], m2_issued[2];
+  uint64_t acc_done, drain, drain2;
   alignas(16) float lse2[8][64];  // read as float4
   alignas(16) float delta[8][64];
   int32_t qpos0[8], qrows[8];
@@ -426,7 +429,7 @@ struct DkvSmemCtl {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kDkvThreads, 1)
     dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const DkvArgs a) {
   using C = DkvCfg<D>;
@@ -451,11 +454,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(&ctl.ring_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&ctl.st_full[i], 1);
-      mbar_init(&ctl.pt_full[i], 8);
+      mbar_init(&ctl.s_full[i], 1);
+      mbar_init(&ctl.dp_full[i], 1);
+      mbar_init(&ctl.p_full[i], 8);
+      mbar_init(&ctl.ds_full[i], 8);
+      mbar_init(&ctl.m2_issued[i], 1);
     }
     mbar_init(&ctl.acc_done, 1);
     mbar_init(&ctl.drain, 1);
+    mbar_init(&ctl.drain2, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -530,67 +537,96 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // MMA issuer: S^T_i = K Q_i^T, dP^T_i = V dO_i^T (SS, N = 64); then
-    // dV += P^T_{i-1} dO_{i-1}, dK += dS^T_{i-1} Q_{i-1} (TS, N = D).  The whole
-    // warp runs the loop (warp-uniform descriptors); one elected lane issues.
+    // first GEMM pair: S^T_i = K Q_i^T, then dP^T_i = V dO_i^T (SS, N = 64), into
+    // TMEM buffer i % 2, each committed on its own barrier.  An issuing thread stalls while the tensor pipe's queue is
+    // full, so the two GEMM pairs have one issuing warp each: while one warp
+    // waits for its next operands, the other's MMAs keep the pipe busy.  The
+    // pair for block i rewrites the buffer that the second pair of block i - 2
+    // reads, so it is issued only after that pair has been issued (m2_issued,
+    // with the tcgen05 thread-sync fences that order the two warps' MMAs).
+    // Both warps run their loops warp-wide (warp-uniform descriptors); one
+    // elected lane issues.
     if (n_iter > 0) {
       constexpr uint32_t idST = idesc_bf16(128, C::BQ, 0, 0);
-      constexpr uint32_t idKV = idesc_bf16(128, D, 0, 1);
       const uint64_t kdesc = sdesc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t vdesc = sdesc_sw128(smem_u32(sV), 16, 1024);
       const uint32_t aRing = smem_u32(sRing);
       bool ok = mbar_wait(&ctl.kv_full, 0, fs);
-      tc_fence_after();
-      for (int i = 0; i <= n_iter && ok; ++i) {
-        if (i < n_iter) {
-          const uint32_t b = i & 1;
-          const int slot = i % C::NST;
-          if (!(ok = mbar_wait(&ctl.ring_full[slot], (i / C::NST) & 1, fs))) break;
-          tc_fence_after();
-          const uint64_t qd = sdesc_sw128(aRing + slot * C::UNIT_BYTES, 16, 1024);
-          const uint64_t dod = sdesc_add(qd, C::QB_BYTES);
-          const uint32_t tS = tmem + C::TM_ST + b * C::BQ, tP = tmem + C::TM_DPT + b * C::BQ;
-          if (elect_one()) {
+      for (int i = 0; i < n_iter && ok; ++i) {
+        const uint32_t b = i & 1;
+        const int slot = i % C::NST;
+        if (!(ok = mbar_wait(&ctl.ring_full[slot], (i / C::NST) & 1, fs))) break;
+        if (i >= 2 && !(ok = mbar_wait(&ctl.m2_issued[b], ((i >> 1) - 1) & 1, fs))) break;
+        tc_fence_after();
+        const uint64_t qd = sdesc_sw128(aRing + slot * C::UNIT_BYTES, 16, 1024);
+        const uint64_t dod = sdesc_add(qd, C::QB_BYTES);
+        const uint32_t tS = tmem + C::TM_ST + b * C::BQ, tP = tmem + C::TM_DPT + b * C::BQ;
+        if (elect_one()) {
+          // S^T first and committed on its own: the compute warps start on P while dP^T runs
 #pragma unroll
-            for (int c = 0; c < C::KCH; ++c)
+          for (int c = 0; c < C::KCH; ++c)
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                mma_bf16_ss(tS, sdesc_add(kdesc, c * C::BN * 128 + k * 32), sdesc_add(qd, c * C::BQ * 128 + k * 32),
-                            idST, (c | k) != 0);
-                mma_bf16_ss(tP, sdesc_add(vdesc, c * C::BN * 128 + k * 32), sdesc_add(dod, c * C::BQ * 128 + k * 32),
-                            idST, (c | k) != 0);
-              }
-            mma_commit(&ctl.st_full[b]);
-          }
-          __syncwarp();
+            for (int k = 0; k < 4; ++k)
+              mma_bf16_ss(tS, sdesc_add(kdesc, c * C::BN * 128 + k * 32), sdesc_add(qd, c * C::BQ * 128 + k * 32),
+                          idST, (c | k) != 0);
+          mma_commit(&ctl.s_full[b]);
+#pragma unroll
+          for (int c = 0; c < C::KCH; ++c)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_bf16_ss(tP, sdesc_add(vdesc, c * C::BN * 128 + k * 32), sdesc_add(dod, c * C::BQ * 128 + k * 32),
+                          idST, (c | k) != 0);
+          mma_commit(&ctl.dp_full[b]);
         }
-        if (i >= 1) {
-          const int ii = i - 1, slot = ii % C::NST;
-          const uint32_t b = ii & 1;
-          if (!(ok = mbar_wait(&ctl.pt_full[b], (ii >> 1) & 1, fs))) break;
-          tc_fence_after();
-          const uint64_t qmn = sdesc_sw128(aRing + slot * C::UNIT_BYTES, C::BQ * 128, 1024);
-          const uint64_t domn = sdesc_add(qmn, C::QB_BYTES);
-          const uint32_t tPT = tmem + C::TM_ST + b * C::BQ, tDST = tmem + C::TM_DPT + b * C::BQ;
-          const uint32_t acc0 = ii > 0 ? 1u : 0u;
-          if (elect_one()) {
+        __syncwarp();
+      }
+      if (elect_one()) mma_commit(&ctl.drain);
+      __syncwarp();
+      mbar_wait_drain(&ctl.drain, 0, kWaitLimitNs);
+    }
+  } else if (warp == 10) {
+    // second GEMM pair: dV += P^T_i dO_i as soon as P^T_i is written, then
+    // dK += dS^T_i Q_i (TS, N = D), A read from the bf16 values the compute
+    // warps wrote over buffer i % 2
+    if (n_iter > 0) {
+      constexpr uint32_t idKV = idesc_bf16(128, D, 0, 1);
+      const uint32_t aRing = smem_u32(sRing);
+      bool ok = true;
+      for (int i = 0; i < n_iter && ok; ++i) {
+        const int slot = i % C::NST;
+        const uint32_t b = i & 1;
+        if (!(ok = mbar_wait(&ctl.p_full[b], (i >> 1) & 1, fs))) break;
+        tc_fence_after();
+        const uint64_t qmn = sdesc_sw128(aRing + slot * C::UNIT_BYTES, C::BQ * 128, 1024);
+        const uint64_t domn = sdesc_add(qmn, C::QB_BYTES);
+        const uint32_t tPT = tmem + C::TM_ST + b * C::BQ, tDST = tmem + C::TM_DPT + b * C::BQ;
+        const uint32_t acc0 = i > 0 ? 1u : 0u;
+        if (elect_one()) {
 #pragma unroll
-            for (int k = 0; k < C::BQ / 16; ++k) {
-              const uint32_t acc = k > 0 ? 1u : acc0;
-              mma_bf16_ts(tmem + C::TM_DV, tPT + packed_kstep_col(k), sdesc_add(domn, k * 16 * 128), idKV, acc);
-              mma_bf16_ts(tmem + C::TM_DK, tDST + packed_kstep_col(k), sdesc_add(qmn, k * 16 * 128), idKV, acc);
-            }
-            mma_commit(&ctl.ring_empty[slot]);
-          }
-          __syncwarp();
+          for (int k = 0; k < C::BQ / 16; ++k)
+            mma_bf16_ts(tmem + C::TM_DV, tPT + packed_kstep_col(k), sdesc_add(domn, k * 16 * 128), idKV,
+                        k > 0 ? 1u : acc0);
         }
+        __syncwarp();
+        if (!(ok = mbar_wait(&ctl.ds_full[b], (i >> 1) & 1, fs))) break;
+        tc_fence_after();
+        if (elect_one()) {
+#pragma unroll
+          for (int k = 0; k < C::BQ / 16; ++k)
+            mma_bf16_ts(tmem + C::TM_DK, tDST + packed_kstep_col(k), sdesc_add(qmn, k * 16 * 128), idKV,
+                        k > 0 ? 1u : acc0);
+          mma_commit(&ctl.ring_empty[slot]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.m2_issued[b]);
       }
       if (elect_one()) {
         if (ok) mma_commit(&ctl.acc_done);
-        mma_commit(&ctl.drain);
+        mma_commit(&ctl.drain2);
       }
       __syncwarp();
-      mbar_wait_drain(&ctl.drain, 0, kWaitLimitNs);
+      mbar_wait_drain(&ctl.drain2, 0, kWaitLimitNs);
     }
   } else {
     // compute warps: thread <-> key row, half <-> 32 query columns of each 64-query block
@@ -604,7 +640,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int i = 0; i < n_iter; ++i) {
       const uint32_t b = i & 1;
       const int slot = i % C::NST;
-      if (!(ok = mbar_wait(&ctl.st_full[b], (i >> 1) & 1, fs))) break;
+      if (!(ok = mbar_wait(&ctl.s_full[b], (i >> 1) & 1, fs))) break;
       // acquire the producer's smem stores of this block (the slot's phase is current:
       // it cannot be refilled before this block's dV/dK MMAs complete)
       if (!(ok = mbar_wait(&ctl.ring_full[slot], (i / C::NST) & 1, fs))) break;
@@ -617,9 +653,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (a.window > 0) chi = min(chi, kpos + a.window - 1 - qpos0);
       if (!kvalid) chi = -1;
       const bool full = (clo <= 0) && (chi >= 31);
-      uint32_t sr[32], dr[32];
+      uint32_t sr[32];
       tmem_ld32(tl + C::TM_ST + b * C::BQ + 32 * half, sr);
-      tmem_ld32(tl + C::TM_DPT + b * C::BQ + 32 * half, dr);
       const float4* L4 = reinterpret_cast<const float4*>(&ctl.lse2[slot][32 * half]);
       const float4* D4 = reinterpret_cast<const float4*>(&ctl.delta[slot][32 * half]);
       tmem_ld_wait();
@@ -629,27 +664,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int c = 0; c < 32; ++c)
           if (c < clo || c > chi) sr[c] = __float_as_uint(-INFINITY);
       }
-      uint32_t wp[16], ws[16];
+      // P^T first: the dV GEMM starts on it while dS^T is computed
+      float p[32];
+      uint32_t wp[16];
 #pragma unroll
       for (int e4 = 0; e4 < 8; ++e4) {
-        const float4 l4 = L4[e4], d4 = D4[e4];
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+        const float4 l4 = L4[e4];
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) p[4 * e4 + e] = ex2_approx(fmaf(__uint_as_float(sr[4 * e4 + e]), sl2, -lv[e]));
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) wp[2 * e4 + e2] = pack_bf16x2(p[4 * e4 + 2 * e2], p[4 * e4 + 2 * e2 + 1]);
+      }
+      tmem_st16(tl + C::TM_ST + b * C::BQ + 32 * half, wp);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.p_full[b]);
+      if (!(ok = mbar_wait(&ctl.dp_full[b], (i >> 1) & 1, fs))) break;
+      tc_fence_after();
+      uint32_t dr[32], ws[16];
+      tmem_ld32(tl + C::TM_DPT + b * C::BQ + 32 * half, dr);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 d4 = D4[e4];
+        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int c = 4 * e4 + 2 * e2;
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lv[2 * e2]));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, -lv[2 * e2 + 1]));
-          wp[2 * e4 + e2] = pack_bf16x2(p0, p1);
-          ws[2 * e4 + e2] = pack_bf16x2(p0 * (__uint_as_float(dr[c]) - dv[2 * e2]),
-                                        p1 * (__uint_as_float(dr[c + 1]) - dv[2 * e2 + 1]));
+          ws[2 * e4 + e2] = pack_bf16x2(p[c] * (__uint_as_float(dr[c]) - dv[2 * e2]),
+                                        p[c + 1] * (__uint_as_float(dr[c + 1]) - dv[2 * e2 + 1]));
         }
       }
-      tmem_st16(tl + C::TM_ST + b * C::BQ + 32 * half, wp);
       tmem_st16(tl + C::TM_DPT + b * C::BQ + 32 * half, ws);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.pt_full[b]);
+      if (lane == 0) mbar_arrive(&ctl.ds_full[b]);
     }
     if (ok) {
       if (n_iter > 0) {
@@ -804,9 +856,9 @@ cudaError_t launch_dkv(int D, const CUtensorMap& tq, const CUtensorMap& tk, cons
   if (n_items <= 0) return cudaSuccess;
   switch (D) {
     case 64:
-      return launch_tc<64, DkvCfg<64>>(dkv_kernel<64>, tq, tk, tv, tdo, a, n_items, st);
+      return launch_tc<64, DkvCfg<64>>(dkv_kernel<64>, tq, tk, tv, tdo, a, n_items, st, kDkvThreads);
     case 128:
-      return launch_tc<128, DkvCfg<128>>(dkv_kernel<128>, tq, tk, tv, tdo, a, n_items, st);
+      return launch_tc<128, DkvCfg<128>>(dkv_kernel<128>, tq, tk, tv, tdo, a, n_items, st, kDkvThreads);
     default:
       return cudaErrorInvalidValue;
   }
