@@ -67,12 +67,16 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepArgs a) {
   }
 }
 
-// Shared structure of the dQ and dK/dV kernels (320 threads):
+// Shared structure of the dQ and dK/dV kernels (352 threads):
 //   warp 0      TMA producer
-//   warp 1      TMEM owner and MMA issuer (one thread; descriptors are computed
-//               once per tile and advanced by constant adds inside unrolled loops)
+//   warp 1      TMEM owner and issuer of the first GEMM pair (S and dP)
+//   warp 10     issuer of the second GEMM pair (dQ, or dV and dK)
 //   warps 2-9   compute: warps w and w+4 share TMEM lane quarter w % 4 (one row
-//               per thread) and split the 64 columns of a block into halves
+//               per thread) and split the columns of a block into halves
+// An issuing thread stalls while the tensor pipe's queue is full; with one
+// issuer per GEMM group the pipe keeps working while either waits for its
+// operands.  Descriptors are computed once per tile and advanced by constant
+// adds inside unrolled loops.
 // The first GEMM pair writes two double-buffered fp32 blocks to TMEM; the
 // compute warps read them, and write the bf16 result (dS, or P^T and dS^T)
 // back over the same buffer, where the second GEMM reads it as its A operand.
@@ -83,7 +87,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepArgs a) {
 // 32 (k / 2) + 8 (k % 2).  tcgen05.mma ops issued by one thread execute in
 // issue order, so a buffer is rewritten by the next first-pair GEMM only
 // after the second GEMM that reads it.
-constexpr int kBwdThreads = 320;
+constexpr int kBwdThreads = 352;
 
 __device__ __forceinline__ uint32_t packed_kstep_col(int k) { return 32u * (k >> 1) + 8u * (k & 1); }
 // The same for halves of 64 values (the dQ kernel's 128-key tiles): half h
@@ -105,7 +109,8 @@ struct DqCfg {
   static constexpr int BM = 128, BN = 128;
   static constexpr int NG = 2;                       // compute warps per TMEM lane quarter
   static constexpr int GC = BN / NG;                 // key columns of one compute warp
-  static constexpr int THREADS = 64 + 128 * NG;
+  static constexpr int THREADS = 96 + 128 * NG;  // producer, two MMA issuers, compute
+  static_assert(THREADS == kBwdThreads, "warp roles assume 11 warps");
   static constexpr int KCH = D / 64;
   static constexpr int Q_BYTES = BM * D * 2;         // Q and dO tiles (resident)
   static constexpr int TILE_BYTES = BN * D * 2;      // one K or V tile
@@ -124,8 +129,8 @@ struct DqCfg {
 struct DqSmemCtl {
   uint64_t q_full;
   uint64_t k_full[6], k_empty[6], v_full[6], v_empty[6];
-  uint64_t s_full, s_empty, dp_empty, ds_full[2], ds_done[2];
-  uint64_t acc_done, drain;
+  uint64_t s_full, dp_full, s_empty, dp_empty, ds_full[2], ds_done[2];
+  uint64_t acc_done, drain, drain2;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -172,6 +177,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       mbar_init(&ctl.v_empty[i], 1);
     }
     mbar_init(&ctl.s_full, 1);
+    mbar_init(&ctl.dp_full, 1);
     mbar_init(&ctl.s_empty, 4 * C::NG);
     mbar_init(&ctl.dp_empty, 4 * C::NG);
     for (int i = 0; i < 2; ++i) {
@@ -180,6 +186,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     }
     mbar_init(&ctl.acc_done, 1);
     mbar_init(&ctl.drain, 1);
+    mbar_init(&ctl.drain2, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -230,75 +237,84 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    // MMA issuer: S_j = Q K_j^T, dP_j = dO V_j^T (SS, N = 128), then dQ += dS_{j-1} K_{j-1} (TS, N = D).
-    // The whole warp runs the loop so descriptors stay warp-uniform; one elected
-    // lane issues each batch of MMAs and its commits.
+    // S_j = Q K_j^T, then dP_j = dO V_j^T (SS, N = 128), each committed on its own
+    // barrier.  A thread issuing tcgen05.mma stalls while the tensor pipe's queue is
+    // full, so dQ has its own issuing warp (warp 10): the two never wait on each
+    // other's operands and write disjoint TMEM.  Both run their loops warp-wide
+    // (warp-uniform descriptors); one elected lane issues.
     if (nt > 0) {
       constexpr uint32_t idS = idesc_bf16(128, C::BN, 0, 0);
-      constexpr uint32_t idQ = idesc_bf16(128, D, 0, 1);
       const uint64_t dQd = sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dDOd = sdesc_sw128(smem_u32(sDO), 16, 1024);
       const uint32_t aKR = smem_u32(sKR), aVR = smem_u32(sVR);
       bool ok = mbar_wait(&ctl.q_full, 0, fs);
-      tc_fence_after();
-      for (int j = 0; j <= nt && ok; ++j) {
-        if (j < nt) {
-          const int ks = j % C::NSK, vs = j % C::NSV;
-          if (!(ok = mbar_wait(&ctl.k_full[ks], (j / C::NSK) & 1, fs))) break;
-          // one S buffer: the compute warps must have loaded S_{j-1}
-          if (j >= 1 && !(ok = mbar_wait(&ctl.s_empty, (j - 1) & 1, fs))) break;
-          tc_fence_after();
-          const uint64_t kd = sdesc_sw128(aKR + ks * C::TILE_BYTES, 16, 1024);
-          if (elect_one()) {
+      for (int j = 0; j < nt && ok; ++j) {
+        const int ks = j % C::NSK, vs = j % C::NSV;
+        if (!(ok = mbar_wait(&ctl.k_full[ks], (j / C::NSK) & 1, fs))) break;
+        // one S buffer: the compute warps must have loaded S_{j-1}
+        if (j >= 1 && !(ok = mbar_wait(&ctl.s_empty, (j - 1) & 1, fs))) break;
+        tc_fence_after();
+        const uint64_t kd = sdesc_sw128(aKR + ks * C::TILE_BYTES, 16, 1024);
+        if (elect_one()) {
 #pragma unroll
-            for (int c = 0; c < C::KCH; ++c)
+          for (int c = 0; c < C::KCH; ++c)
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                mma_bf16_ss(tmem + C::TM_S, sdesc_add(dQd, c * C::BM * 128 + k * 32),
-                            sdesc_add(kd, c * C::BN * 128 + k * 32), idS, (c | k) != 0);
-          }
-          __syncwarp();
-          // one dP buffer: the compute warps must have loaded dP_{j-1}
-          if (!(ok = mbar_wait(&ctl.v_full[vs], (j / C::NSV) & 1, fs))) break;
-          if (j >= 1 && !(ok = mbar_wait(&ctl.dp_empty, (j - 1) & 1, fs))) break;
-          tc_fence_after();
-          const uint64_t vd = sdesc_sw128(aVR + vs * C::TILE_BYTES, 16, 1024);
-          if (elect_one()) {
-#pragma unroll
-            for (int c = 0; c < C::KCH; ++c)
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                mma_bf16_ss(tmem + C::TM_DP, sdesc_add(dDOd, c * C::BM * 128 + k * 32),
-                            sdesc_add(vd, c * C::BN * 128 + k * 32), idS, (c | k) != 0);
-            mma_commit(&ctl.v_empty[vs]);
-            mma_commit(&ctl.s_full);
-          }
-          __syncwarp();
+            for (int k = 0; k < 4; ++k)
+              mma_bf16_ss(tmem + C::TM_S, sdesc_add(dQd, c * C::BM * 128 + k * 32),
+                          sdesc_add(kd, c * C::BN * 128 + k * 32), idS, (c | k) != 0);
+          mma_commit(&ctl.s_full);
         }
-        if (j >= 1) {
-          const int jj = j - 1, ks = jj % C::NSK;
-          const uint32_t b = jj & 1;
-          if (!(ok = mbar_wait(&ctl.ds_full[b], (jj >> 1) & 1, fs))) break;
-          tc_fence_after();
-          const uint64_t kmn = sdesc_sw128(aKR + ks * C::TILE_BYTES, C::BN * 128, 1024);
-          const uint32_t tA = tmem + C::TM_DS + b * (C::BN / 2);
-          const uint32_t acc0 = jj > 0 ? 1u : 0u;
-          if (elect_one()) {
+        __syncwarp();
+        // one dP buffer: the compute warps must have loaded dP_{j-1}
+        if (!(ok = mbar_wait(&ctl.v_full[vs], (j / C::NSV) & 1, fs))) break;
+        if (j >= 1 && !(ok = mbar_wait(&ctl.dp_empty, (j - 1) & 1, fs))) break;
+        tc_fence_after();
+        const uint64_t vd = sdesc_sw128(aVR + vs * C::TILE_BYTES, 16, 1024);
+        if (elect_one()) {
 #pragma unroll
-            for (int k = 0; k < C::BN / 16; ++k)
-              mma_bf16_ts(tmem + C::TM_DQ, tA + 8 * k, sdesc_add(kmn, k * 16 * 128), idQ, k > 0 ? 1u : acc0);
-            mma_commit(&ctl.k_empty[ks]);
-            mma_commit(&ctl.ds_done[b]);
-          }
-          __syncwarp();
+          for (int c = 0; c < C::KCH; ++c)
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_bf16_ss(tmem + C::TM_DP, sdesc_add(dDOd, c * C::BM * 128 + k * 32),
+                          sdesc_add(vd, c * C::BN * 128 + k * 32), idS, (c | k) != 0);
+          mma_commit(&ctl.v_empty[vs]);
+          mma_commit(&ctl.dp_full);
         }
+        __syncwarp();
+      }
+      if (elect_one()) mma_commit(&ctl.drain);
+      __syncwarp();
+      mbar_wait_drain(&ctl.drain, 0, kWaitLimitNs);
+    }
+  } else if (warp == 10) {
+    // dQ += dS_j K_j (TS, N = D): A is the bf16 dS the compute warps wrote into buffer j % 2
+    if (nt > 0) {
+      constexpr uint32_t idQ = idesc_bf16(128, D, 0, 1);
+      const uint32_t aKR = smem_u32(sKR);
+      bool ok = true;
+      for (int j = 0; j < nt && ok; ++j) {
+        const int ks = j % C::NSK;
+        const uint32_t b = j & 1;
+        if (!(ok = mbar_wait(&ctl.ds_full[b], (j >> 1) & 1, fs))) break;
+        tc_fence_after();
+        const uint64_t kmn = sdesc_sw128(aKR + ks * C::TILE_BYTES, C::BN * 128, 1024);
+        const uint32_t tA = tmem + C::TM_DS + b * (C::BN / 2);
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
+        if (elect_one()) {
+#pragma unroll
+          for (int k = 0; k < C::BN / 16; ++k)
+            mma_bf16_ts(tmem + C::TM_DQ, tA + 8 * k, sdesc_add(kmn, k * 16 * 128), idQ, k > 0 ? 1u : acc0);
+          mma_commit(&ctl.k_empty[ks]);
+          mma_commit(&ctl.ds_done[b]);
+        }
+        __syncwarp();
       }
       if (elect_one()) {
         if (ok) mma_commit(&ctl.acc_done);
-        mma_commit(&ctl.drain);
+        mma_commit(&ctl.drain2);
       }
       __syncwarp();
-      mbar_wait_drain(&ctl.drain, 0, kWaitLimitNs);
+      mbar_wait_drain(&ctl.drain2, 0, kWaitLimitNs);
     }
   } else {
     // compute warps: thread <-> query row, group g <-> 32 key columns of each 128-key tile
@@ -327,30 +343,36 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       tc_fence_after();
       uint32_t sr[C::GC], dr[C::GC];
 #pragma unroll
-      for (int c4 = 0; c4 < C::GC / 32; ++c4) {
+      for (int c4 = 0; c4 < C::GC / 32; ++c4)
         tmem_ld32(tl + C::TM_S + C::GC * g + 32 * c4, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c4]));
-        tmem_ld32(tl + C::TM_DP + C::GC * g + 32 * c4, *reinterpret_cast<uint32_t(*)[32]>(&dr[32 * c4]));
-      }
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&ctl.s_empty);
-        mbar_arrive(&ctl.dp_empty);
-      }
+      if (lane == 0) mbar_arrive(&ctl.s_empty);
       // masked keys get S = -inf once (exp2 gives 0); tiles with no masked key skip this
       if (!full) {
 #pragma unroll
         for (int c = 0; c < C::GC; ++c)
           if (c < clo || c > chi) sr[c] = __float_as_uint(-INFINITY);
       }
+      // P while dP_j is still being computed
+      float p[C::GC];
+#pragma unroll
+      for (int c = 0; c < C::GC; ++c) p[c] = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2));
+      if (!(ok = mbar_wait(&ctl.dp_full, j & 1, fs))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c4 = 0; c4 < C::GC / 32; ++c4)
+        tmem_ld32(tl + C::TM_DP + C::GC * g + 32 * c4, *reinterpret_cast<uint32_t(*)[32]>(&dr[32 * c4]));
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.dp_empty);
       uint32_t w[C::GC / 2];
 #pragma unroll
       for (int e = 0; e < C::GC / 2; ++e) {
         const int c = 2 * e;
-        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, -lse2));
-        w[e] = pack_bf16x2(p0 * (__uint_as_float(dr[c]) - delta), p1 * (__uint_as_float(dr[c + 1]) - delta));
+        w[e] = pack_bf16x2(p[c] * (__uint_as_float(dr[c]) - delta), p[c + 1] * (__uint_as_float(dr[c + 1]) - delta));
       }
       // the dS buffer is free once the dQ MMAs of tile j-2 have completed
       if (j >= 2 && !(ok = mbar_wait(&ctl.ds_done[b], ((j - 2) >> 1) & 1, fs))) break;
@@ -413,9 +435,6 @@ struct DkvCfg {
   static constexpr uint32_t TM_ST = 0, TM_DPT = 2 * BQ, TM_DV = 4 * BQ, TM_DK = 4 * BQ + D, TM_COLS = 512;
 };
 
-// dK/dV uses one more warp than the dQ kernel: warp 10 issues the second GEMM pair.
-constexpr int kDkvThreads = kBwdThreads + 32;
-
 struct DkvSmemCtl {
   uint64_t kv_full;
   uint64_t ring_full[8], ring_empty[8];
@@ -429,7 +448,7 @@ struct DkvSmemCtl {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kDkvThreads, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     dkv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const DkvArgs a) {
   using C = DkvCfg<D>;
@@ -856,9 +875,9 @@ cudaError_t launch_dkv(int D, const CUtensorMap& tq, const CUtensorMap& tk, cons
   if (n_items <= 0) return cudaSuccess;
   switch (D) {
     case 64:
-      return launch_tc<64, DkvCfg<64>>(dkv_kernel<64>, tq, tk, tv, tdo, a, n_items, st, kDkvThreads);
+      return launch_tc<64, DkvCfg<64>>(dkv_kernel<64>, tq, tk, tv, tdo, a, n_items, st, kBwdThreads);
     case 128:
-      return launch_tc<128, DkvCfg<128>>(dkv_kernel<128>, tq, tk, tv, tdo, a, n_items, st, kDkvThreads);
+      return launch_tc<128, DkvCfg<128>>(dkv_kernel<128>, tq, tk, tv, tdo, a, n_items, st, kBwdThreads);
     default:
       return cudaErrorInvalidValue;
   }

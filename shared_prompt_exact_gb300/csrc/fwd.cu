@@ -7,14 +7,18 @@
 // (prompt) and then region 1 (own segment), clipped to the causal / window
 // range, with an online softmax.
 //
-// Warp roles (64 + 128 * NH threads):
+// Warp roles (96 + 128 * NH threads):
 //   warp 0      TMA producer: the Q tile once, then K and V tiles through a
 //               ring of "units" (128 rows x 128 head-dim columns, two 64-column
 //               TMA boxes) in the order the MMA warp consumes them
 //               (K_0, K_1, V_0, K_2, V_1, ...)
-//   warp 1      TMEM owner and MMA issuer (whole warp, one elected lane issues):
-//               S_j = Q K_j^T (A and B in shared memory) into one of two TMEM
-//               S buffers; O += P_{j-1} V_{j-1} with P read from TMEM
+//   warp 1      TMEM owner; issues S_j = Q K_j^T (A and B in shared memory)
+//               into one of two TMEM S buffers
+//   warp 2+4NH  issues O += P_j V_j with P read from TMEM.  A thread issuing
+//               tcgen05.mma stalls while the tensor pipe's queue is full, so
+//               each GEMM has its own issuing warp: the pipe keeps working while
+//               either waits for its operands.  Both run their loops warp-wide
+//               (warp-uniform descriptors) and one elected lane issues.
 //   warps 2..    softmax: thread <-> query row (TMEM lane).  With NH = 2 (head
 //               dimension <= 128) each row's 128 key columns are split over two
 //               warps ("halves"); each half keeps its own running max m and sum
@@ -25,8 +29,9 @@
 //               rescales its O when its m grows by more than 2^8 (exact: O and l
 //               share the stale max).  The epilogue combines the halves:
 //               out = (O_0 2^(m_0-m) + O_1 2^(m_1-m)) / (l_0 2^(m_0-m) + l_1 2^(m_1-m)).
-// tcgen05.mma ops issued by one thread execute in issue order, so S_{j+2} is
-// written into the buffer holding P_j only after PV_j, which reads it.
+// S_{j+2} rewrites the buffer holding P_j, so it is issued only after PV_j has
+// been issued (pv_issued, with the tcgen05 thread-sync fences that order the
+// two warps' MMAs).
 //
 // Head dimension 512: the 128 x 512 fp32 O accumulator would fill all of TMEM,
 // so the output columns are split over two CTAs (NSPLIT = 2, 256 columns each);
@@ -46,7 +51,8 @@ struct FwdCfg {
   static constexpr int NSPLIT = (D == 512) ? 2 : 1;
   static constexpr int NH = (D == 512) ? 1 : 2;        // key-column halves per row
   static constexpr int HC = BN / NH;                   // key columns of one half
-  static constexpr int THREADS = 64 + 128 * NH;
+  static constexpr int THREADS = 96 + 128 * NH;
+  static constexpr int PV_WARP = 2 + 4 * NH;           // issuer of the PV GEMMs
   static constexpr int DV = D / NSPLIT;                // output columns of one CTA
   static constexpr int QCH = D / 64;                   // 64-column chunks of Q / K
   static constexpr int UCH = (D == 64) ? 1 : 2;        // chunks per ring unit
@@ -55,6 +61,11 @@ struct FwdCfg {
   static constexpr int VU = (DV / 64) / UCH;           // units per V tile (this CTA's columns)
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int NST = (D == 512) ? 3 : (D == 128 ? 6 : 12);
+  // A ring wait names its fill only by phase parity, so it is exact only if the
+  // slot's previous fill (NST units earlier) has completed.  For V_j that unit
+  // may belong to K_{j+1} when NST < KU + VU; the PV warp then first waits until
+  // the S warp has taken all of K_{j+1} (k_taken).
+  static constexpr bool PV_WAITS_K = NST < KU + VU;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_RING = Q_BYTES;
   static constexpr int SMEM_BYTES = OFF_RING + NST * UNIT_BYTES + 1024;  // + alignment slack
@@ -67,8 +78,8 @@ struct FwdCfg {
 struct FwdSmemCtl {
   uint64_t q_full;
   uint64_t ring_full[12], ring_empty[12];
-  uint64_t s_full[2], p_full[2], pv_done[2];
-  uint64_t drain;
+  uint64_t s_full[2], p_full[2], pv_done[2], pv_issued[2], k_taken[2];
+  uint64_t drain, drain2;
   uint64_t pair_done[4];      // per lane quarter: both halves have published (m, l)
   uint32_t tmem_base;
   int abort_flag;
@@ -115,9 +126,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       mbar_init(&ctl.s_full[i], 1);
       mbar_init(&ctl.p_full[i], 4 * C::NH);
       mbar_init(&ctl.pv_done[i], 1);
+      mbar_init(&ctl.pv_issued[i], 1);
+      mbar_init(&ctl.k_taken[i], 1);
     }
     for (int i = 0; i < 4; ++i) mbar_init(&ctl.pair_done[i], 32 * C::NH);
     mbar_init(&ctl.drain, 1);
+    mbar_init(&ctl.drain2, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -171,68 +185,85 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S issuer
+    // Ring positions follow the producer's order K_0, K_1, V_0, K_2, V_1, ...:
+    // K_j starts at unit KU + (j - 1)(KU + VU) for j >= 1.
     if (nt > 0) {
       constexpr uint32_t idS = idesc_bf16(128, C::BN, 0, 0);
-      constexpr uint32_t idO = idesc_bf16(128, C::UCH * 64, 0, 1);
       const uint64_t qdesc = sdesc_sw128(smem_u32(sQ), 16, 1024);
       const uint32_t aRing = smem_u32(sRing);
-      int idx = 0;
       bool ok = mbar_wait(&ctl.q_full, 0, fs);
-      tc_fence_after();
-      for (int j = 0; j <= nt && ok; ++j) {
-        if (j < nt) {
-          const uint32_t b = j & 1;
-          const uint32_t tS = tmem + C::TM_S + b * C::BN;
-          for (int u = 0; u < C::KU && ok; ++u, ++idx) {
-            const int slot = idx % C::NST;
-            if (!(ok = mbar_wait(&ctl.ring_full[slot], (idx / C::NST) & 1, fs))) break;
-            tc_fence_after();
-            const uint64_t kdesc = sdesc_sw128(aRing + slot * C::UNIT_BYTES, 16, 1024);
-            const uint64_t qd = sdesc_add(qdesc, u * C::UCH * C::BM * 128);
-            if (elect_one()) {
+      for (int j = 0; j < nt && ok; ++j) {
+        const uint32_t b = j & 1;
+        const uint32_t tS = tmem + C::TM_S + b * C::BN;
+        if (j >= 2 && !(ok = mbar_wait(&ctl.pv_issued[b], ((j >> 1) - 1) & 1, fs))) break;
+        int idx = j == 0 ? 0 : C::KU + (j - 1) * (C::KU + C::VU);
+        for (int u = 0; u < C::KU && ok; ++u, ++idx) {
+          const int slot = idx % C::NST;
+          if (!(ok = mbar_wait(&ctl.ring_full[slot], (idx / C::NST) & 1, fs))) break;
+          tc_fence_after();
+          const uint64_t kdesc = sdesc_sw128(aRing + slot * C::UNIT_BYTES, 16, 1024);
+          const uint64_t qd = sdesc_add(qdesc, u * C::UCH * C::BM * 128);
+          if (C::PV_WAITS_K && u == C::KU - 1 && lane == 0) mbar_arrive(&ctl.k_taken[b]);
+          if (elect_one()) {
 #pragma unroll
-              for (int c = 0; c < C::UCH; ++c)
+            for (int c = 0; c < C::UCH; ++c)
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                  mma_bf16_ss(tS, sdesc_add(qd, c * C::BM * 128 + k * 32), sdesc_add(kdesc, c * C::BN * 128 + k * 32),
-                              idS, (u | c | k) != 0);
-              mma_commit(&ctl.ring_empty[slot]);
-              if (u == C::KU - 1) mma_commit(&ctl.s_full[b]);
-            }
-            __syncwarp();
+              for (int k = 0; k < 4; ++k)
+                mma_bf16_ss(tS, sdesc_add(qd, c * C::BM * 128 + k * 32), sdesc_add(kdesc, c * C::BN * 128 + k * 32),
+                            idS, (u | c | k) != 0);
+            mma_commit(&ctl.ring_empty[slot]);
+            if (u == C::KU - 1) mma_commit(&ctl.s_full[b]);
           }
-          if (!ok) break;
-        }
-        if (j >= 1) {
-          const int jj = j - 1;
-          const uint32_t b = jj & 1;
-          if (!(ok = mbar_wait(&ctl.p_full[b], (jj >> 1) & 1, fs))) break;
-          const uint32_t tP = tmem + C::TM_S + b * C::BN;
-          const uint32_t acc0 = jj > 0 ? 1u : 0u;
-          for (int u = 0; u < C::VU && ok; ++u, ++idx) {
-            const int slot = idx % C::NST;
-            if (!(ok = mbar_wait(&ctl.ring_full[slot], (idx / C::NST) & 1, fs))) break;
-            tc_fence_after();
-            const uint64_t vdesc = sdesc_sw128(aRing + slot * C::UNIT_BYTES, C::BN * 128, 1024);
-            if (elect_one()) {
-#pragma unroll
-              for (int h = 0; h < C::NH; ++h)
-#pragma unroll
-                for (int k = 0; k < C::HC / 16; ++k)
-                  mma_bf16_ts(tmem + C::TM_O + h * C::DV + u * C::UCH * 64, tP + h * C::HC + k * 8,
-                              sdesc_add(vdesc, (h * C::HC + k * 16) * 128), idO, k > 0 ? 1u : acc0);
-              mma_commit(&ctl.ring_empty[slot]);
-              if (u == C::VU - 1) mma_commit(&ctl.pv_done[b]);
-            }
-            __syncwarp();
-          }
+          __syncwarp();
         }
       }
       // every MMA issued above must finish before TMEM is released
       if (elect_one()) mma_commit(&ctl.drain);
       __syncwarp();
       mbar_wait_drain(&ctl.drain, 0, kWaitLimitNs);
+    }
+  } else if (warp == C::PV_WARP) {
+    // ------------------------------------------------------------ PV issuer
+    // V_j starts at unit 2 KU + j (KU + VU), except the last tile's, which
+    // follows every K tile and V_0 .. V_{nt-2}: unit nt KU + (nt - 1) VU.
+    if (nt > 0) {
+      constexpr uint32_t idO = idesc_bf16(128, C::UCH * 64, 0, 1);
+      const uint32_t aRing = smem_u32(sRing);
+      bool ok = true;
+      for (int j = 0; j < nt && ok; ++j) {
+        const uint32_t b = j & 1;
+        if (!(ok = mbar_wait(&ctl.p_full[b], (j >> 1) & 1, fs))) break;
+        if (C::PV_WAITS_K && j + 1 < nt &&
+            !(ok = mbar_wait(&ctl.k_taken[(j + 1) & 1], ((j + 1) >> 1) & 1, fs)))
+          break;
+        const uint32_t tP = tmem + C::TM_S + b * C::BN;
+        const uint32_t acc0 = j > 0 ? 1u : 0u;
+        int idx = (j + 1 < nt) ? 2 * C::KU + j * (C::KU + C::VU) : nt * C::KU + (nt - 1) * C::VU;
+        for (int u = 0; u < C::VU && ok; ++u, ++idx) {
+          const int slot = idx % C::NST;
+          if (!(ok = mbar_wait(&ctl.ring_full[slot], (idx / C::NST) & 1, fs))) break;
+          tc_fence_after();
+          const uint64_t vdesc = sdesc_sw128(aRing + slot * C::UNIT_BYTES, C::BN * 128, 1024);
+          if (elect_one()) {
+#pragma unroll
+            for (int h = 0; h < C::NH; ++h)
+#pragma unroll
+              for (int k = 0; k < C::HC / 16; ++k)
+                mma_bf16_ts(tmem + C::TM_O + h * C::DV + u * C::UCH * 64, tP + h * C::HC + k * 8,
+                            sdesc_add(vdesc, (h * C::HC + k * 16) * 128), idO, k > 0 ? 1u : acc0);
+            mma_commit(&ctl.ring_empty[slot]);
+            if (u == C::VU - 1) mma_commit(&ctl.pv_done[b]);
+          }
+          __syncwarp();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.pv_issued[b]);
+      }
+      if (elect_one()) mma_commit(&ctl.drain2);
+      __syncwarp();
+      mbar_wait_drain(&ctl.drain2, 0, kWaitLimitNs);
     }
   } else {
     // ------------------------------------------------------------ softmax
