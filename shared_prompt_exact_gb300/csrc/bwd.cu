@@ -24,7 +24,6 @@ namespace dkv {
 
 namespace {
 
-constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- prep
@@ -90,10 +89,6 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepArgs a) {
 constexpr int kBwdThreads = 352;
 
 __device__ __forceinline__ uint32_t packed_kstep_col(int k) { return 32u * (k >> 1) + 8u * (k & 1); }
-// The same for halves of 64 values (the dQ kernel's 128-key tiles): half h
-// writes its 32 packed columns at [64h, 64h+32), so K-step k (16 keys) sits at
-// column 64 (k / 4) + 8 (k % 4).
-__device__ __forceinline__ uint32_t packed_kstep_col64(int k) { return 64u * (k >> 2) + 8u * (k & 3); }
 
 // ---------------------------------------------------------------- dQ
 // 128-key tiles: S and dP are M=128 x N=128 MMAs.  S and dP each have one TMEM
@@ -104,6 +99,13 @@ __device__ __forceinline__ uint32_t packed_kstep_col64(int k) { return 64u * (k 
 // columns of its query row (two warps per quarter measured fastest: four were
 // slower).
 // TMEM: S 128 | dP 128 | dS 2 x 64 | dQ D columns.
+// The kernel is persistent: CTA c takes work items c, c + grid, c + 2 grid, ...
+// of the cost-sorted list, and the pipeline runs on across items (ring slots
+// and barrier phases follow a tile counter over all of the CTA's tiles), so
+// one item's epilogue overlaps the next item's first GEMMs.  Q and dO of the
+// next item are loaded once every GEMM that reads the current ones is done
+// (q_free), and its first dQ GEMM waits until the compute warps have read the
+// current dQ accumulator (dq_free).
 template <int D>
 struct DqCfg {
   static constexpr int BM = 128, BN = 128;
@@ -129,8 +131,8 @@ struct DqCfg {
 struct DqSmemCtl {
   uint64_t q_full;
   uint64_t k_full[6], k_empty[6], v_full[6], v_empty[6];
-  uint64_t s_full, dp_full, s_empty, dp_empty, ds_full[2], ds_done[2];
-  uint64_t acc_done, drain, drain2;
+  uint64_t q_free, s_full, dp_full, s_empty, dp_empty, ds_full[2], ds_done[2];
+  uint64_t acc_done, dq_free, drain, drain2;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -159,15 +161,16 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
   uint8_t* sKR = smem + C::OFF_KR;
   uint8_t* sVR = smem + C::OFF_VR;
 
-  const QTileItem it = a.items[blockIdx.x];
-  const int nt = (it.reg[0].t_hi - it.reg[0].t_lo) + (it.reg[1].t_hi - it.reg[1].t_lo);
-  const int kvh = it.head / (a.Hq / a.Hkv);
   const uint32_t warp = warp_id(), lane = lane_id();
   FailState fs{&ctl.abort_flag, a.status};
+  auto tiles_of = [](const QTileItem& q) {
+    return (q.reg[0].t_hi - q.reg[0].t_lo) + (q.reg[1].t_hi - q.reg[1].t_lo);
+  };
 
   if (threadIdx.x == 0) {
     ctl.abort_flag = 0;
     mbar_init(&ctl.q_full, 1);
+    mbar_init(&ctl.q_free, 1);
     for (int i = 0; i < C::NSK; ++i) {
       mbar_init(&ctl.k_full[i], 1);
       mbar_init(&ctl.k_empty[i], 1);
@@ -185,6 +188,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       mbar_init(&ctl.ds_done[i], 1);
     }
     mbar_init(&ctl.acc_done, 1);
+    mbar_init(&ctl.dq_free, 4 * C::NG);
     mbar_init(&ctl.drain, 1);
     mbar_init(&ctl.drain2, 1);
     fence_mbar_init();
@@ -198,34 +202,46 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
 
+  // Every role walks the same items; `kx` counts items with at least one key
+  // tile and `g` the tiles over all of them.
   if (warp == 0) {
-    // producer: Q and dO once, then K_j (K ring) and V_j (V ring)
-    if (lane == 0 && nt > 0) {
-      mbar_arrive_expect_tx(&ctl.q_full, 2 * C::Q_BYTES);
-      for (int c = 0; c < C::KCH; ++c) {
-        tma_load_3d(sQ + c * C::BM * 128, &tmQ, &ctl.q_full, c * 64, it.head, it.q_row0);
-        tma_load_3d(sDO + c * C::BM * 128, &tmDO, &ctl.q_full, c * 64, it.head, it.q_row0);
-      }
+    // producer: per item Q and dO, then K_j (K ring) and V_j (V ring)
+    if (lane == 0) {
       bool ok = true;
-      int j = 0, nk = 0, nv = 0;
-      for (; j < nt && ok; ++j) {
-        int r, t;
-        qtile_of(it, j, r, t);
-        const int key_row = it.reg[r].row0 + t * C::BN;
-        const int ks = j % C::NSK, vs = j % C::NSV;
-        if (!(ok = mbar_wait(&ctl.k_empty[ks], ((j / C::NSK) & 1) ^ 1, fs))) break;
-        mbar_arrive_expect_tx(&ctl.k_full[ks], C::TILE_BYTES);
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_3d(sKR + ks * C::TILE_BYTES + c * C::BN * 128, &tmK, &ctl.k_full[ks], c * 64, kvh, key_row);
-        ++nk;
-        if (!(ok = mbar_wait(&ctl.v_empty[vs], ((j / C::NSV) & 1) ^ 1, fs))) break;
-        mbar_arrive_expect_tx(&ctl.v_full[vs], C::TILE_BYTES);
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_3d(sVR + vs * C::TILE_BYTES + c * C::BN * 128, &tmV, &ctl.v_full[vs], c * 64, kvh, key_row);
-        ++nv;
+      int g = 0, kx = 0, nk = 0, nv = 0;
+      for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
+        const QTileItem it = a.items[item];
+        const int nt = tiles_of(it);
+        if (nt == 0) continue;
+        const int kvh = it.head / (a.Hq / a.Hkv);
+        // Q / dO are overwritten only after every GEMM of the previous item has completed
+        if (kx > 0 && !(ok = mbar_wait(&ctl.q_free, (kx - 1) & 1, fs))) break;
+        mbar_arrive_expect_tx(&ctl.q_full, 2 * C::Q_BYTES);
+        for (int c = 0; c < C::KCH; ++c) {
+          tma_load_3d(sQ + c * C::BM * 128, &tmQ, &ctl.q_full, c * 64, it.head, it.q_row0);
+          tma_load_3d(sDO + c * C::BM * 128, &tmDO, &ctl.q_full, c * 64, it.head, it.q_row0);
+        }
+        ++kx;
+        for (int j = 0; j < nt && ok; ++j, ++g) {
+          int r, t;
+          qtile_of(it, j, r, t);
+          const int key_row = it.reg[r].row0 + t * C::BN;
+          const int ks = g % C::NSK, vs = g % C::NSV;
+          if (!(ok = mbar_wait(&ctl.k_empty[ks], ((g / C::NSK) & 1) ^ 1, fs))) break;
+          mbar_arrive_expect_tx(&ctl.k_full[ks], C::TILE_BYTES);
+          for (int c = 0; c < C::KCH; ++c)
+            tma_load_3d(sKR + ks * C::TILE_BYTES + c * C::BN * 128, &tmK, &ctl.k_full[ks], c * 64, kvh, key_row);
+          ++nk;
+          if (!(ok = mbar_wait(&ctl.v_empty[vs], ((g / C::NSV) & 1) ^ 1, fs))) break;
+          mbar_arrive_expect_tx(&ctl.v_full[vs], C::TILE_BYTES);
+          for (int c = 0; c < C::KCH; ++c)
+            tma_load_3d(sVR + vs * C::TILE_BYTES + c * C::BN * 128, &tmV, &ctl.v_full[vs], c * 64, kvh, key_row);
+          ++nv;
+        }
       }
       if (!ok) {
-        mbar_wait_drain(&ctl.q_full, 0, kWaitLimitNs);
+        // drain: wait for the copies still in flight before the CTA can exit
+        if (kx > 0) mbar_wait_drain(&ctl.q_full, (kx - 1) & 1, kWaitLimitNs);
         for (int back = 1; back <= C::NSK && back <= nk; ++back) {
           const int i2 = nk - back;
           mbar_wait_drain(&ctl.k_full[i2 % C::NSK], (i2 / C::NSK) & 1, kWaitLimitNs);
@@ -242,17 +258,22 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     // full, so dQ has its own issuing warp (warp 10): the two never wait on each
     // other's operands and write disjoint TMEM.  Both run their loops warp-wide
     // (warp-uniform descriptors); one elected lane issues.
-    if (nt > 0) {
-      constexpr uint32_t idS = idesc_bf16(128, C::BN, 0, 0);
-      const uint64_t dQd = sdesc_sw128(smem_u32(sQ), 16, 1024);
-      const uint64_t dDOd = sdesc_sw128(smem_u32(sDO), 16, 1024);
-      const uint32_t aKR = smem_u32(sKR), aVR = smem_u32(sVR);
-      bool ok = mbar_wait(&ctl.q_full, 0, fs);
-      for (int j = 0; j < nt && ok; ++j) {
-        const int ks = j % C::NSK, vs = j % C::NSV;
-        if (!(ok = mbar_wait(&ctl.k_full[ks], (j / C::NSK) & 1, fs))) break;
-        // one S buffer: the compute warps must have loaded S_{j-1}
-        if (j >= 1 && !(ok = mbar_wait(&ctl.s_empty, (j - 1) & 1, fs))) break;
+    constexpr uint32_t idS = idesc_bf16(128, C::BN, 0, 0);
+    const uint64_t dQd = sdesc_sw128(smem_u32(sQ), 16, 1024);
+    const uint64_t dDOd = sdesc_sw128(smem_u32(sDO), 16, 1024);
+    const uint32_t aKR = smem_u32(sKR), aVR = smem_u32(sVR);
+    bool ok = true;
+    int g = 0, kx = 0;
+    for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
+      const int nt = tiles_of(a.items[item]);
+      if (nt == 0) continue;
+      if (!(ok = mbar_wait(&ctl.q_full, kx & 1, fs))) break;
+      ++kx;
+      for (int j = 0; j < nt && ok; ++j, ++g) {
+        const int ks = g % C::NSK, vs = g % C::NSV;
+        if (!(ok = mbar_wait(&ctl.k_full[ks], (g / C::NSK) & 1, fs))) break;
+        // one S buffer: the compute warps must have loaded the previous S
+        if (g >= 1 && !(ok = mbar_wait(&ctl.s_empty, (g - 1) & 1, fs))) break;
         tc_fence_after();
         const uint64_t kd = sdesc_sw128(aKR + ks * C::TILE_BYTES, 16, 1024);
         if (elect_one()) {
@@ -265,9 +286,9 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
           mma_commit(&ctl.s_full);
         }
         __syncwarp();
-        // one dP buffer: the compute warps must have loaded dP_{j-1}
-        if (!(ok = mbar_wait(&ctl.v_full[vs], (j / C::NSV) & 1, fs))) break;
-        if (j >= 1 && !(ok = mbar_wait(&ctl.dp_empty, (j - 1) & 1, fs))) break;
+        // one dP buffer: the compute warps must have loaded the previous dP
+        if (!(ok = mbar_wait(&ctl.v_full[vs], (g / C::NSV) & 1, fs))) break;
+        if (g >= 1 && !(ok = mbar_wait(&ctl.dp_empty, (g - 1) & 1, fs))) break;
         tc_fence_after();
         const uint64_t vd = sdesc_sw128(aVR + vs * C::TILE_BYTES, 16, 1024);
         if (elect_one()) {
@@ -279,23 +300,29 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
                           sdesc_add(vd, c * C::BN * 128 + k * 32), idS, (c | k) != 0);
           mma_commit(&ctl.v_empty[vs]);
           mma_commit(&ctl.dp_full);
+          if (j == nt - 1) mma_commit(&ctl.q_free);  // this item's Q and dO are no longer read
         }
         __syncwarp();
       }
-      if (elect_one()) mma_commit(&ctl.drain);
-      __syncwarp();
-      mbar_wait_drain(&ctl.drain, 0, kWaitLimitNs);
     }
+    if (elect_one()) mma_commit(&ctl.drain);
+    __syncwarp();
+    mbar_wait_drain(&ctl.drain, 0, kWaitLimitNs);
   } else if (warp == 10) {
-    // dQ += dS_j K_j (TS, N = D): A is the bf16 dS the compute warps wrote into buffer j % 2
-    if (nt > 0) {
-      constexpr uint32_t idQ = idesc_bf16(128, D, 0, 1);
-      const uint32_t aKR = smem_u32(sKR);
-      bool ok = true;
-      for (int j = 0; j < nt && ok; ++j) {
-        const int ks = j % C::NSK;
-        const uint32_t b = j & 1;
-        if (!(ok = mbar_wait(&ctl.ds_full[b], (j >> 1) & 1, fs))) break;
+    // dQ += dS_j K_j (TS, N = D): A is the bf16 dS the compute warps wrote into buffer g % 2
+    constexpr uint32_t idQ = idesc_bf16(128, D, 0, 1);
+    const uint32_t aKR = smem_u32(sKR);
+    bool ok = true;
+    int g = 0, kx = 0;
+    for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
+      const int nt = tiles_of(a.items[item]);
+      if (nt == 0) continue;
+      for (int j = 0; j < nt && ok; ++j, ++g) {
+        const int ks = g % C::NSK;
+        const uint32_t b = g & 1;
+        if (!(ok = mbar_wait(&ctl.ds_full[b], (g >> 1) & 1, fs))) break;
+        // the accumulator is reused once the previous item's dQ has been read out
+        if (j == 0 && kx > 0 && !(ok = mbar_wait(&ctl.dq_free, (kx - 1) & 1, fs))) break;
         tc_fence_after();
         const uint64_t kmn = sdesc_sw128(aKR + ks * C::TILE_BYTES, C::BN * 128, 1024);
         const uint32_t tA = tmem + C::TM_DS + b * (C::BN / 2);
@@ -306,110 +333,124 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
             mma_bf16_ts(tmem + C::TM_DQ, tA + 8 * k, sdesc_add(kmn, k * 16 * 128), idQ, k > 0 ? 1u : acc0);
           mma_commit(&ctl.k_empty[ks]);
           mma_commit(&ctl.ds_done[b]);
+          if (j == nt - 1) mma_commit(&ctl.acc_done);
         }
         __syncwarp();
       }
-      if (elect_one()) {
-        if (ok) mma_commit(&ctl.acc_done);
-        mma_commit(&ctl.drain2);
-      }
-      __syncwarp();
-      mbar_wait_drain(&ctl.drain2, 0, kWaitLimitNs);
+      ++kx;
     }
+    if (elect_one()) mma_commit(&ctl.drain2);
+    __syncwarp();
+    mbar_wait_drain(&ctl.drain2, 0, kWaitLimitNs);
   } else {
-    // compute warps: thread <-> query row, group g <-> 32 key columns of each 128-key tile
-    const uint32_t wq = warp & 3, g = (warp - 2) >> 2;
+    // compute warps: thread <-> query row, group g <-> 64 key columns of each 128-key tile
+    const uint32_t wq = warp & 3, grp = (warp - 2) >> 2;
     const int row = (int)(wq * 32 + lane);
     const uint32_t tl = tmem + ((wq * 32) << 16);
-    const int qpos = it.q_pos0 + row;
-    const bool valid = row < it.q_rows;
-    const int64_t rix = (int64_t)it.head * a.T + it.q_row0 + row;
-    const float lse2 = valid ? a.lse2[rix] : INFINITY;  // P = 0 on rows past the tile
-    const float delta = valid ? a.delta[rix] : 0.f;
     const float sl2 = a.scale_log2;
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-      const uint32_t b = j & 1;
-      int r, t;
-      qtile_of(it, j, r, t);
-      const KeyRegion& kr = it.reg[r];
-      const int kl0 = t * C::BN + C::GC * (int)g;
-      int lo = 0;
-      if (a.window > 0) lo = max(0, qpos - a.window + 1 - kr.pos0);
-      const int hi = min(kr.count - 1, qpos - kr.pos0);
-      const int clo = lo - kl0, chi = hi - kl0;  // allowed columns of this group
-      const bool full = (clo <= 0) && (chi >= C::GC - 1);
-      if (!(ok = mbar_wait(&ctl.s_full, j & 1, fs))) break;
-      tc_fence_after();
-      uint32_t sr[C::GC], dr[C::GC];
+    int g = 0, kx = 0;
+    for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
+      const QTileItem it = a.items[item];
+      const int nt = tiles_of(it);
+      const int qpos = it.q_pos0 + row;
+      const bool valid = row < it.q_rows;
+      // this warp writes dQ columns [grp * D / NG, (grp + 1) * D / NG) of its row
+      constexpr int OC = D / C::NG;
+      __nv_bfloat16* qrow = a.dq + ((int64_t)(it.q_row0 + row) * a.Hq + it.head) * D;
+      if (nt == 0) {
+        // no key at all: dQ = 0
+        if (valid) {
 #pragma unroll
-      for (int c4 = 0; c4 < C::GC / 32; ++c4)
-        tmem_ld32(tl + C::TM_S + C::GC * g + 32 * c4, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c4]));
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.s_empty);
-      // masked keys get S = -inf once (exp2 gives 0); tiles with no masked key skip this
-      if (!full) {
-#pragma unroll
-        for (int c = 0; c < C::GC; ++c)
-          if (c < clo || c > chi) sr[c] = __float_as_uint(-INFINITY);
+          for (int v = 0; v < OC / 8; ++v) reinterpret_cast<uint4*>(qrow + grp * OC)[v] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        continue;
       }
-      // P while dP_j is still being computed
-      float p[C::GC];
+      const int64_t rix = (int64_t)it.head * a.T + it.q_row0 + row;
+      const float lse2 = valid ? a.lse2[rix] : INFINITY;  // P = 0 on rows past the tile
+      const float delta = valid ? a.delta[rix] : 0.f;
+      for (int j = 0; j < nt; ++j, ++g) {
+        const uint32_t b = g & 1;
+        int r, t;
+        qtile_of(it, j, r, t);
+        const KeyRegion& kr = it.reg[r];
+        const int kl0 = t * C::BN + C::GC * (int)grp;
+        int lo = 0;
+        if (a.window > 0) lo = max(0, qpos - a.window + 1 - kr.pos0);
+        const int hi = min(kr.count - 1, qpos - kr.pos0);
+        const int clo = lo - kl0, chi = hi - kl0;  // allowed columns of this group
+        const bool full = (clo <= 0) && (chi >= C::GC - 1);
+        if (!(ok = mbar_wait(&ctl.s_full, g & 1, fs))) break;
+        tc_fence_after();
+        uint32_t sr[C::GC], dr[C::GC];
 #pragma unroll
-      for (int c = 0; c < C::GC; ++c) p[c] = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2));
-      if (!(ok = mbar_wait(&ctl.dp_full, j & 1, fs))) break;
-      tc_fence_after();
+        for (int c4 = 0; c4 < C::GC / 32; ++c4)
+          tmem_ld32(tl + C::TM_S + C::GC * grp + 32 * c4, *reinterpret_cast<uint32_t(*)[32]>(&sr[32 * c4]));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.s_empty);
+        // masked keys get S = -inf once (exp2 gives 0); tiles with no masked key skip this
+        if (!full) {
 #pragma unroll
-      for (int c4 = 0; c4 < C::GC / 32; ++c4)
-        tmem_ld32(tl + C::TM_DP + C::GC * g + 32 * c4, *reinterpret_cast<uint32_t(*)[32]>(&dr[32 * c4]));
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.dp_empty);
-      uint32_t w[C::GC / 2];
+          for (int c = 0; c < C::GC; ++c)
+            if (c < clo || c > chi) sr[c] = __float_as_uint(-INFINITY);
+        }
+        // P while dP is still being computed
+        float p[C::GC];
 #pragma unroll
-      for (int e = 0; e < C::GC / 2; ++e) {
-        const int c = 2 * e;
-        w[e] = pack_bf16x2(p[c] * (__uint_as_float(dr[c]) - delta), p[c + 1] * (__uint_as_float(dr[c + 1]) - delta));
+        for (int c = 0; c < C::GC; ++c) p[c] = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2));
+        if (!(ok = mbar_wait(&ctl.dp_full, g & 1, fs))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c4 = 0; c4 < C::GC / 32; ++c4)
+          tmem_ld32(tl + C::TM_DP + C::GC * grp + 32 * c4, *reinterpret_cast<uint32_t(*)[32]>(&dr[32 * c4]));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.dp_empty);
+        uint32_t w[C::GC / 2];
+#pragma unroll
+        for (int e = 0; e < C::GC / 2; ++e) {
+          const int c = 2 * e;
+          w[e] = pack_bf16x2(p[c] * (__uint_as_float(dr[c]) - delta), p[c + 1] * (__uint_as_float(dr[c + 1]) - delta));
+        }
+        // the dS buffer is free once the dQ MMAs of the tile two back have completed
+        if (g >= 2 && !(ok = mbar_wait(&ctl.ds_done[b], ((g - 2) >> 1) & 1, fs))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c4 = 0; c4 < C::GC / 32; ++c4)
+          tmem_st16(tl + C::TM_DS + b * (C::BN / 2) + (C::GC / 2) * grp + 16 * c4,
+                    *reinterpret_cast<const uint32_t(*)[16]>(&w[16 * c4]));
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.ds_full[b]);
       }
-      // the dS buffer is free once the dQ MMAs of tile j-2 have completed
-      if (j >= 2 && !(ok = mbar_wait(&ctl.ds_done[b], ((j - 2) >> 1) & 1, fs))) break;
+      if (!ok) break;
+      // epilogue: dQ = scale * accumulator, then release the accumulator
+      if (!(ok = mbar_wait(&ctl.acc_done, kx & 1, fs))) break;
       tc_fence_after();
 #pragma unroll
-      for (int c4 = 0; c4 < C::GC / 32; ++c4)
-        tmem_st16(tl + C::TM_DS + b * (C::BN / 2) + (C::GC / 2) * g + 16 * c4,
-                  *reinterpret_cast<const uint32_t(*)[16]>(&w[16 * c4]));
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.ds_full[b]);
-    }
-    if (ok && nt > 0) {
-      ok = mbar_wait(&ctl.acc_done, 0, fs);
-      tc_fence_after();
-      if (ok) {
-        // this warp writes dQ columns [g * D / NG, (g + 1) * D / NG) of its rows
-        constexpr int OC = D / C::NG;
-        __nv_bfloat16* qrow = a.dq + ((int64_t)(it.q_row0 + row) * a.Hq + it.head) * D;
+      for (int c4 = 0; c4 < (OC + 31) / 32; ++c4) {
+        const int col = (int)grp * OC + c4 * 32;
+        uint32_t rr[32];
+        tmem_ld32(tl + C::TM_DQ + col, rr);
+        tmem_ld_wait();
+        uint32_t o[16];
 #pragma unroll
-        for (int c4 = 0; c4 < (OC + 31) / 32; ++c4) {
-          const int col = (int)g * OC + c4 * 32;
-          uint32_t rr[32];
-          tmem_ld32(tl + C::TM_DQ + col, rr);
-          tmem_ld_wait();
-          uint32_t o[16];
+        for (int i = 0; i < 16; ++i)
+          o[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * a.scale, __uint_as_float(rr[2 * i + 1]) * a.scale);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(qrow + col);
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            o[i] = pack_bf16x2(__uint_as_float(rr[2 * i]) * a.scale, __uint_as_float(rr[2 * i + 1]) * a.scale);
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(qrow + col);
-#pragma unroll
-            for (int v = 0; v < OC / 8 && v < 4; ++v) dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
-          }
+          for (int v = 0; v < OC / 8 && v < 4; ++v) dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.dq_free);
+      ++kx;
     }
   }
   tc_fence_before();
@@ -860,11 +901,18 @@ static cudaError_t launch_tc(K kernel, const CUtensorMap& t0, const CUtensorMap&
 cudaError_t launch_dq(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                       const CUtensorMap& tdo, const DqArgs& a, int n_items, cudaStream_t st) {
   if (n_items <= 0) return cudaSuccess;
+  // persistent: one CTA per SM, each walking every grid-th item
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidValue;
+  DqArgs b = a;
+  b.n_items = n_items;
+  const int grid = n_items < nsm ? n_items : nsm;
   switch (D) {
     case 64:
-      return launch_tc<64, DqCfg<64>>(dq_kernel<64>, tq, tk, tv, tdo, a, n_items, st, DqCfg<64>::THREADS);
+      return launch_tc<64, DqCfg<64>>(dq_kernel<64>, tq, tk, tv, tdo, b, grid, st, DqCfg<64>::THREADS);
     case 128:
-      return launch_tc<128, DqCfg<128>>(dq_kernel<128>, tq, tk, tv, tdo, a, n_items, st, DqCfg<128>::THREADS);
+      return launch_tc<128, DqCfg<128>>(dq_kernel<128>, tq, tk, tv, tdo, b, grid, st, DqCfg<128>::THREADS);
     default:
       return cudaErrorInvalidValue;
   }

@@ -45,6 +45,7 @@ struct DqArgs {
   float scale_log2;  // softmax scale * log2(e)
   float scale;       // softmax scale
   uint32_t* status;
+  int n_items = 0;   // set by launch_dq
 };
 int dq_query_tile(int D);
 int dq_key_tile(int D);
