@@ -415,8 +415,12 @@ def run_dualkv(args, w):
                                              "ms_per_group": ms_h / W}
     dualkv.dualkv_check_status(stream)
 
-    # end to end through the C ABI with host buffers: pinned H2D of the step's
-    # inputs, forward + backward, D2H of every output
+    # end to end through the C ABI with host buffers: every step uploads its q, k, v, dO
+    # from pinned host memory and downloads out, lse, dq, dk, dv.  As in a training
+    # loop that prefetches its next micro-batch, device buffers are double-buffered:
+    # uploads run on their own stream (dO's overlaps the forward, the next step's
+    # overlap this step's backward), downloads on another (out and lse overlap the
+    # backward).  Every copy lies inside the timed region.
     e2e = None
     if not args.no_e2e:
         pin = lambda x: x.pin_memory()  # noqa: E731
@@ -424,20 +428,77 @@ def run_dualkv(args, w):
         ho, hl, hdq, hdk, hdv = (torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (out, lse, dq, dk, dv))
         h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
         d2h = sum(x.numel() * x.element_size() for x in (ho, hl, hdq, hdk, hdv))
+        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        dins = [(q, k, v, do)] + [tuple(torch.empty_like(x) for x in (q, k, v, do))]
+        douts = [(out, lse, dq, dk, dv)] + [tuple(torch.empty_like(x) for x in (out, lse, dq, dk, dv))]
+        in_free, out_free = [None, None], [None, None]
 
-        def e2e_step():
-            q.copy_(hq, non_blocking=True)
-            k.copy_(hk, non_blocking=True)
-            v.copy_(hv, non_blocking=True)
-            do.copy_(hdo, non_blocking=True)
-            step()
-            for hdst, src in ((ho, out), (hl, lse), (hdq, dq), (hdk, dk), (hdv, dv)):
-                hdst.copy_(src, non_blocking=True)
+        def e2e_step(i):
+            bsel = i & 1
+            qd, kd, vd, dod = dins[bsel]
+            od, ld, dqd, dkd, dvd = douts[bsel]
+            with torch.cuda.stream(up):
+                if in_free[bsel] is not None:
+                    up.wait_event(in_free[bsel])
+                qd.copy_(hq, non_blocking=True)
+                kd.copy_(hk, non_blocking=True)
+                vd.copy_(hv, non_blocking=True)
+                e_qkv = torch.cuda.Event()
+                e_qkv.record(up)
+                dod.copy_(hdo, non_blocking=True)
+                e_do = torch.cuda.Event()
+                e_do.record(up)
+            stream.wait_event(e_qkv)
+            if out_free[bsel] is not None:
+                stream.wait_event(out_free[bsel])
+            dualkv.dualkv_fwd(qd, kd, vd, w.P, w.N, w.offsets, Hq, Hkv, D, w.scale, w.window, od, ld, stream)
+            e_fwd = torch.cuda.Event()
+            e_fwd.record(stream)
+            stream.wait_event(e_do)
+            dualkv.dualkv_bwd(qd, kd, vd, od, ld, dod, w.P, w.N, w.offsets, Hq, Hkv, D, w.scale, w.window, dqd, dkd,
+                              dvd, ws, None, stream)
+            e_bwd = torch.cuda.Event()
+            e_bwd.record(stream)
+            in_free[bsel] = e_bwd
+            with torch.cuda.stream(down):
+                down.wait_event(e_fwd)
+                ho.copy_(od, non_blocking=True)
+                hl.copy_(ld, non_blocking=True)
+                down.wait_event(e_bwd)
+                hdq.copy_(dqd, non_blocking=True)
+                hdk.copy_(dkd, non_blocking=True)
+                hdv.copy_(dvd, non_blocking=True)
+                e_out = torch.cuda.Event()
+                e_out.record(down)
+                out_free[bsel] = e_out
 
-        e2e_step()
-        ms_e2e = max_over_ranks(timed(e2e_step, max(1, min(args.steps, 5))), world, dev)
+        def timed_e2e(reps):
+            barrier(world)
+            torch.cuda.synchronize(dev)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            up.wait_event(e0)
+            down.wait_event(e0)
+            for i in range(reps):
+                e2e_step(i)
+            stream.wait_stream(up)
+            stream.wait_stream(down)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            barrier(world)
+            return e0.elapsed_time(e1) / reps
+
+        e2e_step(0)
+        e2e_step(1)
+        torch.cuda.synchronize(dev)
+        ms_e2e = max_over_ranks(timed_e2e(max(2, min(args.steps, 10))), world, dev)
+        dualkv.dualkv_check_status(stream)
         e2e = {"value": world * f_step / (ms_e2e * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e}
+               "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
+               "pipelining": "double-buffered device inputs/outputs; uploads and downloads on their own streams"}
+        dins.clear()
+        douts.clear()
 
     # the same kernels on the replicated layout (prompt copied into every sequence)
     replicated = None
