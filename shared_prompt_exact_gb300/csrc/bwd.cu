@@ -398,8 +398,13 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         }
         // P while dP is still being computed
         float p[C::GC];
+        const float2 sl2v = make_float2(sl2, sl2), nl = make_float2(-lse2, -lse2);
 #pragma unroll
-        for (int c = 0; c < C::GC; ++c) p[c] = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2));
+        for (int c = 0; c < C::GC; c += 2) {
+          const float2 x = ffma2(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2v, nl);
+          p[c] = ex2_approx(x.x);
+          p[c + 1] = ex2_approx(x.y);
+        }
         if (!(ok = mbar_wait(&ctl.dp_full, g & 1, fs))) break;
         tc_fence_after();
 #pragma unroll
@@ -410,10 +415,13 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&ctl.dp_empty);
         uint32_t w[C::GC / 2];
+        const float2 dl = make_float2(delta, delta);
 #pragma unroll
         for (int e = 0; e < C::GC / 2; ++e) {
           const int c = 2 * e;
-          w[e] = pack_bf16x2(p[c] * (__uint_as_float(dr[c]) - delta), p[c + 1] * (__uint_as_float(dr[c + 1]) - delta));
+          const float2 ds = fmul2(make_float2(p[c], p[c + 1]),
+                                  fsub2(make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), dl));
+          w[e] = pack_bf16x2(ds.x, ds.y);
         }
         // the dS buffer is free once the dQ MMAs of the tile two back have completed
         if (g >= 2 && !(ok = mbar_wait(&ctl.ds_done[b], ((g - 2) >> 1) & 1, fs))) break;
@@ -727,14 +735,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // P^T first: the dV GEMM starts on it while dS^T is computed
       float p[32];
       uint32_t wp[16];
+      const float2 sl2v = make_float2(sl2, sl2);
 #pragma unroll
       for (int e4 = 0; e4 < 8; ++e4) {
         const float4 l4 = L4[e4];
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        const float2 nl[2] = {make_float2(-l4.x, -l4.y), make_float2(-l4.z, -l4.w)};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) p[4 * e4 + e] = ex2_approx(fmaf(__uint_as_float(sr[4 * e4 + e]), sl2, -lv[e]));
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) wp[2 * e4 + e2] = pack_bf16x2(p[4 * e4 + 2 * e2], p[4 * e4 + 2 * e2 + 1]);
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int c = 4 * e4 + 2 * e2;
+          const float2 x = ffma2(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), sl2v, nl[e2]);
+          p[c] = ex2_approx(x.x);
+          p[c + 1] = ex2_approx(x.y);
+          wp[2 * e4 + e2] = pack_bf16x2(p[c], p[c + 1]);
+        }
       }
       tmem_st16(tl + C::TM_ST + b * C::BQ + 32 * half, wp);
       tmem_st_wait();
@@ -749,12 +762,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
       for (int e4 = 0; e4 < 8; ++e4) {
         const float4 d4 = D4[e4];
-        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+        const float2 dv[2] = {make_float2(d4.x, d4.y), make_float2(d4.z, d4.w)};
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int c = 4 * e4 + 2 * e2;
-          ws[2 * e4 + e2] = pack_bf16x2(p[c] * (__uint_as_float(dr[c]) - dv[2 * e2]),
-                                        p[c + 1] * (__uint_as_float(dr[c + 1]) - dv[2 * e2 + 1]));
+          const float2 ds = fmul2(make_float2(p[c], p[c + 1]),
+                                  fsub2(make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), dv[e2]));
+          ws[2 * e4 + e2] = pack_bf16x2(ds.x, ds.y);
         }
       }
       tmem_st16(tl + C::TM_DPT + b * C::BQ + 32 * half, ws);

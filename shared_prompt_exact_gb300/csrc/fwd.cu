@@ -300,17 +300,18 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
       }
       tmem_ld_wait();
 
-      float mx = -INFINITY;
-      if (full) {
+      if (!full) {
 #pragma unroll
-        for (int c = 0; c < C::HC; ++c) mx = fmaxf(mx, s[c]);
-      } else {
-#pragma unroll
-        for (int c = 0; c < C::HC; ++c) {
-          s[c] = (c < clo || c > chi) ? -INFINITY : s[c];
-          mx = fmaxf(mx, s[c]);
-        }
+        for (int c = 0; c < C::HC; ++c) s[c] = (c < clo || c > chi) ? -INFINITY : s[c];
       }
+      // row max: four independent chains of three-input max
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < C::HC; c += 8) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) mq[q4] = fmax3(mq[q4], s[c + 2 * q4], s[c + 2 * q4 + 1]);
+      }
+      const float mx = fmax3(fmaxf(mq[0], mq[1]), mq[2], mq[3]);
       const float m_tile = mx * sl2;  // -inf stays -inf (sl2 > 0)
       const float m_new = fmaxf(m, m_tile);
       if (j == 0) {
@@ -335,21 +336,23 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         m = m_new;
       }
       const float m_use = (m == -INFINITY) ? 0.f : m;
-      float sum = 0.f;
+      const float2 sl2v = make_float2(sl2, sl2), negm = make_float2(-m_use, -m_use);
+      float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int h2 = 0; h2 < C::HC / 64; ++h2) {
         uint32_t w[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int c = h2 * 64 + 2 * e;
-          const float p0 = ex2_approx(fmaf(s[c], sl2, -m_use));
-          const float p1 = ex2_approx(fmaf(s[c + 1], sl2, -m_use));
-          sum += p0 + p1;
-          w[e] = pack_bf16x2(p0, p1);
+          const float2 x = ffma2(make_float2(s[c], s[c + 1]), sl2v, negm);
+          const float2 pp = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          sum2[e & 1] = fadd2(sum2[e & 1], pp);
+          w[e] = pack_bf16x2(pp.x, pp.y);
         }
         tmem_st32(tl + C::TM_S + b * C::BN + half * C::HC + h2 * 32, w);
       }
-      l += sum;
+      const float2 st = fadd2(sum2[0], sum2[1]);
+      l += st.x + st.y;
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
