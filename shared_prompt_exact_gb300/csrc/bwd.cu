@@ -125,13 +125,16 @@ struct DqCfg {
   static constexpr int OFF_KR = OFF_DO + Q_BYTES;
   static constexpr int OFF_VR = OFF_KR + NSK * TILE_BYTES;
   static constexpr int SMEM_BYTES = OFF_VR + NSV * TILE_BYTES + 1024;
-  static constexpr uint32_t TM_S = 0, TM_DP = BN, TM_DS = 2 * BN, TM_DQ = 3 * BN, TM_COLS = 512;
+  // TMEM: S | dP (BN columns each) | dS (BN / 2 packed, single buffer) | Q (D / 2: A operand of S) | dQ (D)
+  static constexpr uint32_t TM_S = 0, TM_DP = BN, TM_DS = 2 * BN, TM_Q = 2 * BN + BN / 2, TM_DQ = 3 * BN,
+                            TM_COLS = 512;
+  static_assert(TM_Q + D / 2 <= TM_DQ && TM_DQ + D <= TM_COLS, "TMEM budget");
 };
 
 struct DqSmemCtl {
   uint64_t q_full;
   uint64_t k_full[6], k_empty[6], v_full[6], v_empty[6];
-  uint64_t q_free, s_full, dp_full, s_empty, dp_empty, ds_full[2], ds_done[2];
+  uint64_t q_free, q_tmem, s_full, dp_full, s_empty, dp_empty, ds_full, ds_done;
   uint64_t acc_done, dq_free, drain, drain2;
   uint32_t tmem_base;
   int abort_flag;
@@ -171,6 +174,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     ctl.abort_flag = 0;
     mbar_init(&ctl.q_full, 1);
     mbar_init(&ctl.q_free, 1);
+    mbar_init(&ctl.q_tmem, 4 * C::NG);
     for (int i = 0; i < C::NSK; ++i) {
       mbar_init(&ctl.k_full[i], 1);
       mbar_init(&ctl.k_empty[i], 1);
@@ -183,10 +187,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     mbar_init(&ctl.dp_full, 1);
     mbar_init(&ctl.s_empty, 4 * C::NG);
     mbar_init(&ctl.dp_empty, 4 * C::NG);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&ctl.ds_full[i], 4 * C::NG);
-      mbar_init(&ctl.ds_done[i], 1);
-    }
+    mbar_init(&ctl.ds_full, 4 * C::NG);
+    mbar_init(&ctl.ds_done, 1);
     mbar_init(&ctl.acc_done, 1);
     mbar_init(&ctl.dq_free, 4 * C::NG);
     mbar_init(&ctl.drain, 1);
@@ -259,7 +261,6 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     // other's operands and write disjoint TMEM.  Both run their loops warp-wide
     // (warp-uniform descriptors); one elected lane issues.
     constexpr uint32_t idS = idesc_bf16(128, C::BN, 0, 0);
-    const uint64_t dQd = sdesc_sw128(smem_u32(sQ), 16, 1024);
     const uint64_t dDOd = sdesc_sw128(smem_u32(sDO), 16, 1024);
     const uint32_t aKR = smem_u32(sKR), aVR = smem_u32(sVR);
     bool ok = true;
@@ -267,7 +268,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
       const int nt = tiles_of(a.items[item]);
       if (nt == 0) continue;
-      if (!(ok = mbar_wait(&ctl.q_full, kx & 1, fs))) break;
+      // Q copied into TMEM (after its TMA load, which also brought dO)
+      if (!(ok = mbar_wait(&ctl.q_tmem, kx & 1, fs))) break;
       ++kx;
       for (int j = 0; j < nt && ok; ++j, ++g) {
         const int ks = g % C::NSK, vs = g % C::NSV;
@@ -281,8 +283,8 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
           for (int c = 0; c < C::KCH; ++c)
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_bf16_ss(tmem + C::TM_S, sdesc_add(dQd, c * C::BM * 128 + k * 32),
-                          sdesc_add(kd, c * C::BN * 128 + k * 32), idS, (c | k) != 0);
+              mma_bf16_ts(tmem + C::TM_S, tmem + C::TM_Q + 8 * (4 * c + k), sdesc_add(kd, c * C::BN * 128 + k * 32),
+                          idS, (c | k) != 0);
           mma_commit(&ctl.s_full);
         }
         __syncwarp();
@@ -319,20 +321,19 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       if (nt == 0) continue;
       for (int j = 0; j < nt && ok; ++j, ++g) {
         const int ks = g % C::NSK;
-        const uint32_t b = g & 1;
-        if (!(ok = mbar_wait(&ctl.ds_full[b], (g >> 1) & 1, fs))) break;
+        if (!(ok = mbar_wait(&ctl.ds_full, g & 1, fs))) break;
         // the accumulator is reused once the previous item's dQ has been read out
         if (j == 0 && kx > 0 && !(ok = mbar_wait(&ctl.dq_free, (kx - 1) & 1, fs))) break;
         tc_fence_after();
         const uint64_t kmn = sdesc_sw128(aKR + ks * C::TILE_BYTES, C::BN * 128, 1024);
-        const uint32_t tA = tmem + C::TM_DS + b * (C::BN / 2);
+        const uint32_t tA = tmem + C::TM_DS;
         const uint32_t acc0 = j > 0 ? 1u : 0u;
         if (elect_one()) {
 #pragma unroll
           for (int k = 0; k < C::BN / 16; ++k)
             mma_bf16_ts(tmem + C::TM_DQ, tA + 8 * k, sdesc_add(kmn, k * 16 * 128), idQ, k > 0 ? 1u : acc0);
           mma_commit(&ctl.k_empty[ks]);
-          mma_commit(&ctl.ds_done[b]);
+          mma_commit(&ctl.ds_done);
           if (j == nt - 1) mma_commit(&ctl.acc_done);
         }
         __syncwarp();
@@ -369,8 +370,28 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       const int64_t rix = (int64_t)it.head * a.T + it.q_row0 + row;
       const float lse2 = valid ? a.lse2[rix] : INFINITY;  // P = 0 on rows past the tile
       const float delta = valid ? a.delta[rix] : 0.f;
+      // copy this item's Q tile from shared memory into TMEM, the A operand of S:
+      // group g copies 64-column chunks g, g + NG, ... of its row.  The previous
+      // item's S GEMMs have completed (their results were loaded above).
+      if (!(ok = mbar_wait(&ctl.q_full, kx & 1, fs))) break;
+#pragma unroll
+      for (int c = (int)grp; c < C::KCH; c += C::NG) {
+        uint32_t w[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 x = *reinterpret_cast<const uint4*>(sQ + c * C::BM * 128 + sw128_offset((uint32_t)row, u));
+          w[4 * u] = x.x;
+          w[4 * u + 1] = x.y;
+          w[4 * u + 2] = x.z;
+          w[4 * u + 3] = x.w;
+        }
+        tmem_st32(tl + C::TM_Q + 32 * c, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.q_tmem);
       for (int j = 0; j < nt; ++j, ++g) {
-        const uint32_t b = g & 1;
         int r, t;
         qtile_of(it, j, r, t);
         const KeyRegion& kr = it.reg[r];
@@ -423,17 +444,16 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
                                   fsub2(make_float2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])), dl));
           w[e] = pack_bf16x2(ds.x, ds.y);
         }
-        // the dS buffer is free once the dQ MMAs of the tile two back have completed
-        if (g >= 2 && !(ok = mbar_wait(&ctl.ds_done[b], ((g - 2) >> 1) & 1, fs))) break;
+        // the dS buffer is free once the dQ MMAs of the previous tile have completed
+        if (g >= 1 && !(ok = mbar_wait(&ctl.ds_done, (g - 1) & 1, fs))) break;
         tc_fence_after();
 #pragma unroll
         for (int c4 = 0; c4 < C::GC / 32; ++c4)
-          tmem_st16(tl + C::TM_DS + b * (C::BN / 2) + (C::GC / 2) * grp + 16 * c4,
-                    *reinterpret_cast<const uint32_t(*)[16]>(&w[16 * c4]));
+          tmem_st16(tl + C::TM_DS + (C::GC / 2) * grp + 16 * c4, *reinterpret_cast<const uint32_t(*)[16]>(&w[16 * c4]));
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.ds_full[b]);
+        if (lane == 0) mbar_arrive(&ctl.ds_full);
       }
       if (!ok) break;
       // epilogue: dQ = scale * accumulator, then release the accumulator
