@@ -849,22 +849,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 // ---------------------------------------------------------------- reduce
 // dK, dV of a split key tile = sum over its chunks s = 0..nslots-1 in order.
-__global__ void __launch_bounds__(256) reduce_kernel(const ReduceArgs a) {
+// Block (item, y) covers key rows [y * R, (y + 1) * R) of the item with
+// R = 1024 / D, one float4 of dK and of dV per thread; the chunks' loads are
+// independent, so several are in flight per thread.  HBM-bound.
+constexpr int kReduceThreads = 256;
+__global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceArgs a) {
   const ReduceItem it = a.items[blockIdx.x];
-  const int n = it.k_rows * a.D;
+  const int v4_per_row = a.D / 4;
+  const int e4 = blockIdx.y * kReduceThreads + threadIdx.x;  // float4 index inside the tile
+  const int j = e4 / v4_per_row, d = (e4 % v4_per_row) * 4;
+  if (j >= it.k_rows) return;
   const size_t slot_stride = (size_t)2 * a.key_tile * a.D;
-  for (int e = threadIdx.x; e < n; e += blockDim.x) {
-    const int j = e / a.D, d = e % a.D;
-    float sk = 0.f, sv = 0.f;
-    for (int s = 0; s < it.nslots; ++s) {
-      const float* base = a.partial + (size_t)(it.slot0 + s) * slot_stride;
-      sk += base[(size_t)j * a.D + d];
-      sv += base[(size_t)a.key_tile * a.D + (size_t)j * a.D + d];
-    }
-    const int64_t o = ((int64_t)(it.k_row0 + j) * a.Hkv + it.kv_head) * a.D + d;
-    a.dk[o] = __float2bfloat16_rn(sk);
-    a.dv[o] = __float2bfloat16_rn(sv);
+  const float* base = a.partial + (size_t)it.slot0 * slot_stride + (size_t)j * a.D + d;
+  float4 sk = make_float4(0.f, 0.f, 0.f, 0.f), sv = sk;
+#pragma unroll 4
+  for (int s = 0; s < it.nslots; ++s) {
+    const float4 k4 = *reinterpret_cast<const float4*>(base + (size_t)s * slot_stride);
+    const float4 v4 = *reinterpret_cast<const float4*>(base + (size_t)s * slot_stride + (size_t)a.key_tile * a.D);
+    sk.x += k4.x; sk.y += k4.y; sk.z += k4.z; sk.w += k4.w;
+    sv.x += v4.x; sv.y += v4.y; sv.z += v4.z; sv.w += v4.w;
   }
+  const int64_t o = ((int64_t)(it.k_row0 + j) * a.Hkv + it.kv_head) * a.D + d;
+  *reinterpret_cast<uint2*>(a.dk + o) = make_uint2(pack_bf16x2(sk.x, sk.y), pack_bf16x2(sk.z, sk.w));
+  *reinterpret_cast<uint2*>(a.dv + o) = make_uint2(pack_bf16x2(sv.x, sv.y), pack_bf16x2(sv.z, sv.w));
 }
 
 // ---------------------------------------------------------------- failure-path self-test
@@ -967,7 +974,9 @@ cudaError_t launch_dkv(int D, const CUtensorMap& tq, const CUtensorMap& tk, cons
 
 cudaError_t launch_reduce(const ReduceArgs& a, int n_items, cudaStream_t st) {
   if (n_items <= 0) return cudaSuccess;
-  reduce_kernel<<<n_items, 256, 0, st>>>(a);
+  // key_tile rows x D floats per item, 4 floats per thread
+  const unsigned gy = (unsigned)((a.key_tile * a.D / 4 + kReduceThreads - 1) / kReduceThreads);
+  reduce_kernel<<<dim3((unsigned)n_items, gy), kReduceThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
 
