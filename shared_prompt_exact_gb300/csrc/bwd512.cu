@@ -57,8 +57,11 @@ struct PdsCtl {
 };
 
 // MODE 0: A = Q, B = K, writes P blocks.  MODE 1: A = dO, B = V, reads P, writes dS blocks.
+// Warps 2-9 convert S: warps w and w+4 share TMEM lane quarter w % 4 (one query
+// row per thread) and take key columns [0, 64) and [64, 128) of each block.
+constexpr int kPdsThreads = 320;
 template <int MODE>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kPdsThreads, 1)
     pds_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const PdsArgs a) {
   using C = PdsCfg;
   extern __shared__ uint8_t smem_raw[];
@@ -83,7 +86,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl.s_full[i], 1);
-      mbar_init(&ctl.s_empty[i], 4);
+      mbar_init(&ctl.s_empty[i], 8);
     }
     mbar_init(&ctl.drain, 1);
     fence_mbar_init();
@@ -160,8 +163,8 @@ __global__ void __launch_bounds__(192, 1)
       mbar_wait_drain(&ctl.drain, 0, kWaitLimitNs);
     }
   } else {
-    // thread <-> query row; each tile yields one 256-byte row of the output block
-    const uint32_t wq = warp & 3;
+    // thread <-> query row, half <-> 64 key columns; each tile yields 128 bytes of one row of the output block
+    const uint32_t wq = warp & 3, half = (warp - 2) >> 2;
     const int row = (int)(wq * 32 + lane);
     const uint32_t tl = tmem + ((wq * 32) << 16);
     const int qpos = it.q_pos0 + row;
@@ -169,16 +172,17 @@ __global__ void __launch_bounds__(192, 1)
     const int64_t rix = (int64_t)it.head * a.T + it.q_row0 + row;
     const float lse2 = (MODE == 0 && valid) ? a.lse2[rix] : INFINITY;
     const float delta = (MODE == 1 && valid) ? a.delta[rix] : 0.f;
+    constexpr int HC = C::BN / 2;
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       const uint32_t b = j & 1;
       if (!(ok = mbar_wait(&ctl.s_full[b], (j >> 1) & 1, fs))) break;
       tc_fence_after();
-      float s[C::BN];
+      float s[HC];
 #pragma unroll
-      for (int c4 = 0; c4 < C::BN / 32; ++c4) {
+      for (int c4 = 0; c4 < HC / 32; ++c4) {
         uint32_t rr[32];
-        tmem_ld32(tl + b * C::BN + c4 * 32, rr);
+        tmem_ld32(tl + b * C::BN + HC * half + c4 * 32, rr);
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[c4 * 32 + i] = __uint_as_float(rr[i]);
       }
@@ -186,25 +190,27 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.s_empty[b]);
-      const size_t boff = (size_t)(blk0 + j) * (kBlkBytes / 2) + (size_t)row * C::BN;
+      const size_t boff = (size_t)(blk0 + j) * (kBlkBytes / 2) + (size_t)row * C::BN + HC * half;
       uint4* dst = reinterpret_cast<uint4*>(a.out_blocks + boff);
       if (MODE == 0) {
         int r, t;
         walk_tile(it, j, r, t);
         const KeyRegion& kr = it.reg[r];
-        const int kl0 = t * C::BN;
+        const int kl0 = t * C::BN + HC * (int)half;
         int lo = 0;
         if (a.window > 0) lo = max(0, qpos - a.window + 1 - kr.pos0);
         const int hi = min(kr.count - 1, qpos - kr.pos0);
         const int clo = lo - kl0, chi = hi - kl0;
+        const float2 sl2v = make_float2(a.scale_log2, a.scale_log2), nl = make_float2(-lse2, -lse2);
 #pragma unroll
-        for (int v = 0; v < C::BN / 8; ++v) {
+        for (int v = 0; v < HC / 8; ++v) {
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int c = 8 * v + 2 * e;
-            float p0 = ex2_approx(fmaf(s[c], a.scale_log2, -lse2));
-            float p1 = ex2_approx(fmaf(s[c + 1], a.scale_log2, -lse2));
+            const float2 x = ffma2(make_float2(s[c], s[c + 1]), sl2v, nl);
+            float p0 = ex2_approx(x.x);
+            float p1 = ex2_approx(x.y);
             p0 = (c < clo || c > chi) ? 0.f : p0;
             p1 = (c + 1 < clo || c + 1 > chi) ? 0.f : p1;
             w[e] = pack_bf16x2(p0, p1);
@@ -213,16 +219,17 @@ __global__ void __launch_bounds__(192, 1)
         }
       } else {
         const uint4* src = reinterpret_cast<const uint4*>(a.p_blocks + boff);
+        const float2 dl = make_float2(delta, delta);
 #pragma unroll
-        for (int v = 0; v < C::BN / 8; ++v) {
+        for (int v = 0; v < HC / 8; ++v) {
           const uint4 pin = src[v];
           const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&pin);
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int c = 8 * v + 2 * e;
-            const float2 p = __bfloat1622float2(p2[e]);
-            w[e] = pack_bf16x2(p.x * (s[c] - delta), p.y * (s[c + 1] - delta));
+            const float2 ds = fmul2(__bfloat1622float2(p2[e]), fsub2(make_float2(s[c], s[c + 1]), dl));
+            w[e] = pack_bf16x2(ds.x, ds.y);
           }
           dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
         }
@@ -536,10 +543,10 @@ cudaError_t launch_pds(int mode, const CUtensorMap& tA, const CUtensorMap& tB, c
   cudaError_t e;
   if (mode == 0) {
     if ((e = set_smem(pds_kernel<0>, PdsCfg::SMEM_BYTES, s0)) != cudaSuccess) return e;
-    pds_kernel<0><<<n_items, 192, PdsCfg::SMEM_BYTES, st>>>(tA, tB, a);
+    pds_kernel<0><<<n_items, kPdsThreads, PdsCfg::SMEM_BYTES, st>>>(tA, tB, a);
   } else {
     if ((e = set_smem(pds_kernel<1>, PdsCfg::SMEM_BYTES, s1)) != cudaSuccess) return e;
-    pds_kernel<1><<<n_items, 192, PdsCfg::SMEM_BYTES, st>>>(tA, tB, a);
+    pds_kernel<1><<<n_items, kPdsThreads, PdsCfg::SMEM_BYTES, st>>>(tA, tB, a);
   }
   return cudaGetLastError();
 }
