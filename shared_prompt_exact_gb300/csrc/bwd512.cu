@@ -36,20 +36,26 @@ __device__ __forceinline__ void walk_tile(const QTileItem& it, int j, int& r, in
 }
 
 // ---------------------------------------------------------------- P / dS blocks
+// The resident operand (Q or dO, 128 rows x 512) is an A operand in TMEM: it
+// lands by TMA in the ring's shared memory, the compute warps copy it into
+// TMEM, and the ring then streams K / V tiles.  Only B is read from shared
+// memory by the MMAs, and the ring is 7 units deep.
 struct PdsCfg {
   static constexpr int BM = 128, BN = 128;
   static constexpr int QCH = kD / 64;          // chunks of the resident operand
   static constexpr int UNIT_BYTES = 2 * BN * 128;  // two 64-column chunks of a key tile
   static constexpr int KU = QCH / 2;           // units per key tile
-  static constexpr int A_BYTES = BM * kD * 2;  // 128 KB
-  static constexpr int NST = 3;
-  static constexpr int SMEM_BYTES = A_BYTES + NST * UNIT_BYTES + 1024;
-  static constexpr uint32_t TM_COLS = 256;     // two S buffers
+  static constexpr int A_BYTES = BM * kD * 2;  // 128 KB, staged in the ring before the first key tile
+  static constexpr int NST = 7;
+  static_assert(A_BYTES <= NST * UNIT_BYTES, "A is staged in the ring");
+  static constexpr int SMEM_BYTES = NST * UNIT_BYTES + 1024;
+  static constexpr uint32_t TM_A = 2 * BN;     // after the two S buffers: kD / 2 columns
+  static constexpr uint32_t TM_COLS = 512;
 };
 
 struct PdsCtl {
-  uint64_t a_full;
-  uint64_t ring_full[3], ring_empty[3];
+  uint64_t a_full, a_tmem;
+  uint64_t ring_full[7], ring_empty[7];
   uint64_t s_full[2], s_empty[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -67,8 +73,8 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ PdsCtl ctl;
-  uint8_t* sA = smem;
-  uint8_t* sRing = smem + C::A_BYTES;
+  uint8_t* sRing = smem;
+  uint8_t* sA = smem;  // staging of the resident operand, before the ring is used
 
   const QTileItem it = a.items[blockIdx.x];
   const int blk0 = a.block_base[blockIdx.x];
@@ -80,6 +86,7 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
   if (threadIdx.x == 0) {
     ctl.abort_flag = 0;
     mbar_init(&ctl.a_full, 1);
+    mbar_init(&ctl.a_tmem, 8);
     for (int i = 0; i < C::NST; ++i) {
       mbar_init(&ctl.ring_full[i], 1);
       mbar_init(&ctl.ring_empty[i], 1);
@@ -105,12 +112,13 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
       mbar_arrive_expect_tx(&ctl.a_full, C::A_BYTES);
       for (int c = 0; c < C::QCH; ++c) tma_load_3d(sA + c * C::BM * 128, &tmA, &ctl.a_full, c * 64, it.head, it.q_row0);
       int idx = 0;
-      bool ok = true;
+      // the ring reuses the staging memory once the compute warps have copied A into TMEM
+      bool ok = mbar_wait(&ctl.a_tmem, 0, fs);
       for (int j = 0; j < nt && ok; ++j) {
         int r, t;
         walk_tile(it, j, r, t);
         const int key_row = it.reg[r].row0 + t * C::BN;
-        for (int u = 0; u < C::KU; ++u, ++idx) {
+        for (int u = 0; u < C::KU && ok; ++u, ++idx) {
           const int slot = idx % C::NST;
           if (!(ok = mbar_wait(&ctl.ring_empty[slot], ((idx / C::NST) & 1) ^ 1, fs))) break;
           mbar_arrive_expect_tx(&ctl.ring_full[slot], C::UNIT_BYTES);
@@ -130,9 +138,8 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
   } else if (warp == 1) {
     if (nt > 0) {
       constexpr uint32_t idS = idesc_bf16(128, C::BN, 0, 0);
-      const uint64_t adesc = sdesc_sw128(smem_u32(sA), 16, 1024);
       const uint32_t aRing = smem_u32(sRing);
-      bool ok = mbar_wait(&ctl.a_full, 0, fs);
+      bool ok = mbar_wait(&ctl.a_tmem, 0, fs);  // A copied into TMEM
       tc_fence_after();
       int idx = 0;
       for (int j = 0; j < nt && ok; ++j) {
@@ -144,13 +151,12 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
           if (!(ok = mbar_wait(&ctl.ring_full[slot], (idx / C::NST) & 1, fs))) break;
           tc_fence_after();
           const uint64_t bdesc = sdesc_sw128(aRing + slot * C::UNIT_BYTES, 16, 1024);
-          const uint64_t ad = sdesc_add(adesc, u * 2 * C::BM * 128);
           if (elect_one()) {
 #pragma unroll
             for (int c = 0; c < 2; ++c)
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_bf16_ss(tS, sdesc_add(ad, c * C::BM * 128 + k * 32), sdesc_add(bdesc, c * C::BN * 128 + k * 32),
+                mma_bf16_ts(tS, tmem + C::TM_A + 8 * ((2 * u + c) * 4 + k), sdesc_add(bdesc, c * C::BN * 128 + k * 32),
                             idS, (u | c | k) != 0);
             mma_commit(&ctl.ring_empty[slot]);
             if (u == C::KU - 1) mma_commit(&ctl.s_full[b]);
@@ -174,8 +180,40 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
     const float delta = (MODE == 1 && valid) ? a.delta[rix] : 0.f;
     constexpr int HC = C::BN / 2;
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
+    if (nt > 0) {
+      // copy this row of the resident operand into TMEM (the A operand of the
+      // GEMM): the first half's warps take 64-column chunks 0-3, the second's 4-7
+      if ((ok = mbar_wait(&ctl.a_full, 0, fs))) {
+#pragma unroll
+        for (int cc = 0; cc < C::QCH / 2; ++cc) {
+          const int c = (int)half * (C::QCH / 2) + cc;
+          uint32_t w[32];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint4 x = *reinterpret_cast<const uint4*>(sA + c * C::BM * 128 + sw128_offset((uint32_t)row, u));
+            w[4 * u] = x.x;
+            w[4 * u + 1] = x.y;
+            w[4 * u + 2] = x.z;
+            w[4 * u + 3] = x.w;
+          }
+          tmem_st32(tl + C::TM_A + 32 * c, w);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.a_tmem);
+      }
+    }
+    for (int j = 0; j < nt && ok; ++j) {
       const uint32_t b = j & 1;
+      const size_t boff = (size_t)(blk0 + j) * (kBlkBytes / 2) + (size_t)row * C::BN + HC * half;
+      // dS needs this block's P: its loads are issued before waiting for S
+      uint4 pin[HC / 8];
+      if (MODE == 1) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.p_blocks + boff);
+#pragma unroll
+        for (int v = 0; v < HC / 8; ++v) pin[v] = src[v];
+      }
       if (!(ok = mbar_wait(&ctl.s_full[b], (j >> 1) & 1, fs))) break;
       tc_fence_after();
       float s[HC];
@@ -190,7 +228,6 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.s_empty[b]);
-      const size_t boff = (size_t)(blk0 + j) * (kBlkBytes / 2) + (size_t)row * C::BN + HC * half;
       uint4* dst = reinterpret_cast<uint4*>(a.out_blocks + boff);
       if (MODE == 0) {
         int r, t;
@@ -218,12 +255,10 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
           dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
         }
       } else {
-        const uint4* src = reinterpret_cast<const uint4*>(a.p_blocks + boff);
         const float2 dl = make_float2(delta, delta);
 #pragma unroll
         for (int v = 0; v < HC / 8; ++v) {
-          const uint4 pin = src[v];
-          const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&pin);
+          const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&pin[v]);
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
