@@ -67,10 +67,19 @@ def peaks():
         return dict(bf16_burst=1900.0, bf16_sustained=1700.0, hbm_gbs=6800.0, source="fallback")
 
 
-def source_digest():
+# source files each timed kernel kind is built from (its kernel, the shared device
+# helpers, the work-list planner and the launch code)
+_COMMON_SOURCES = ["ptx.cuh", "kernels.h", "plan.h", "plan.cpp", "api.cu"]
+KERNEL_SOURCES = {"fwd": ["fwd.cu"] + _COMMON_SOURCES, "dkv": ["bwd.cu"] + _COMMON_SOURCES,
+                  "dq": ["bwd.cu"] + _COMMON_SOURCES}
+
+
+def source_digest(kernel=None):
+    """Digest of the sources of `kernel` (a KERNEL_SOURCES key), or of every source."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "shared_prompt_exact_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    names = KERNEL_SOURCES[kernel] if kernel else sorted(os.listdir(csrc))
+    for name in names:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -78,14 +87,14 @@ def source_digest():
 
 
 def ncu_traffic(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, if taken on the current sources."""
+    """DRAM bytes per launch from the committed ncu summary, if taken on the kernel's current sources."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}_ncu.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     s = re.search(r"source_digest:\s*([0-9a-f]+)", text)
-    if not m or not s or s.group(1) != source_digest():
+    if not m or not s or s.group(1) != source_digest(kernel if kernel in KERNEL_SOURCES else None):
         return None
     return float(m.group(1))
 
