@@ -198,6 +198,22 @@ def max_over_ranks(x, world, device):
     return float(t.item())
 
 
+def sum_over_ranks(x, world, device):
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate_strong(ms_local, flops_local, world, device):
+    """Whole-job throughput when the ranks split one step's work (head sharding):
+    total work over the slowest rank's time."""
+    ms = max_over_ranks(ms_local, world, device)
+    return ms, sum_over_ranks(flops_local, world, device) / (ms * 1e-3) / 1e12
+
+
 def aggregate(ms_local, flops_per_rank, world, device):
     """Whole-job throughput of `world` independent replicas: every rank does
     flops_per_rank per step; the job's step time is the slowest rank's."""
@@ -336,12 +352,33 @@ def run_dualkv(args, w):
     ws = dualkv.workspace_for(w.P, w.offsets, Hq, Hkv, D, w.window, dev)
     stream = torch.cuda.current_stream(dev)
 
+    # --shard heads: every rank computes its own contiguous group of kv-heads of the
+    # same micro-batch through the head-range entry points (the layout a
+    # head-sharded sequence-parallel rank holds after its exchange); no collective
+    shard = args.shard == "heads" and world > 1
+    klo, khi = dualkv.kv_head_ranges(Hkv, world)[rank] if shard else (0, Hkv)
+    head_frac = (khi - klo) / Hkv
+
+    def run_fwd(q_, k_, v_, out_, lse_):
+        if not shard:
+            dualkv.dualkv_fwd(q_, k_, v_, w.P, w.N, w.offsets, Hq, Hkv, D, w.scale, w.window, out_, lse_, stream)
+        elif khi > klo:
+            dualkv.dualkv_fwd_heads(q_, k_, v_, w.P, w.N, w.offsets, Hq, Hkv, D, w.scale, w.window, klo, khi, out_,
+                                    lse_, stream)
+
+    def run_bwd(q_, k_, v_, out_, lse_, do_, dq_, dk_, dv_):
+        if not shard:
+            dualkv.dualkv_bwd(q_, k_, v_, out_, lse_, do_, w.P, w.N, w.offsets, Hq, Hkv, D, w.scale, w.window, dq_,
+                              dk_, dv_, ws, None, stream)
+        elif khi > klo:
+            dualkv.dualkv_bwd_heads(q_, k_, v_, out_, lse_, do_, w.P, w.N, w.offsets, Hq, Hkv, D, w.scale, w.window,
+                                    klo, khi, dq_, dk_, dv_, ws, None, stream)
+
     def fwd():
-        dualkv.dualkv_fwd(q, k, v, w.P, w.N, w.offsets, Hq, Hkv, D, w.scale, w.window, out, lse, stream)
+        run_fwd(q, k, v, out, lse)
 
     def bwd():
-        dualkv.dualkv_bwd(q, k, v, out, lse, do, w.P, w.N, w.offsets, Hq, Hkv, D, w.scale, w.window, dq, dk, dv, ws,
-                          None, stream)
+        run_bwd(q, k, v, out, lse, do, dq, dk, dv)
 
     def step():
         fwd()
@@ -374,7 +411,10 @@ def run_dualkv(args, w):
     t_start = time.time()
     ms_step = timed(step, args.steps)
     t_end = time.time()
-    ms_step, value = aggregate(ms_step, f_step, world, dev)
+    if shard:
+        ms_step, value = aggregate_strong(ms_step, f_step * head_frac, world, dev)
+    else:
+        ms_step, value = aggregate(ms_step, f_step, world, dev)
     ms_fwd = max_over_ranks(timed(fwd, args.steps), world, dev)
     ms_bwd = max_over_ranks(timed(bwd, args.steps), world, dev)
     dualkv.dualkv_check_status(stream)
@@ -392,8 +432,8 @@ def run_dualkv(args, w):
     dom = max(kt, key=lambda kk: kt[kk][0])
     pk = peaks()
     roofline = None
-    if dom in KERNEL_FLOPS_PER_PAIR:
-        per_launch_flops = KERNEL_FLOPS_PER_PAIR[dom] * D * Hq * pairs
+    if dom in KERNEL_FLOPS_PER_PAIR and kt[dom][1] > 0:
+        per_launch_flops = KERNEL_FLOPS_PER_PAIR[dom] * D * Hq * pairs * head_frac
         avg_ms = kt[dom][0] / kt[dom][1]
         achieved = per_launch_flops / (avg_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": pk["bf16_sustained"],
@@ -406,7 +446,7 @@ def run_dualkv(args, w):
     # the same step as W head-range calls of Hkv / W kv-heads each (the per-rank
     # share of a W-way head split), run back to back on this GPU
     head_groups = {}
-    for W in (2, Hkv):
+    for W in (() if shard else (2, Hkv)):
         if W < 2 or Hkv % W:
             continue
         ranges = [(i * Hkv // W, (i + 1) * Hkv // W) for i in range(W)]
@@ -460,12 +500,11 @@ def run_dualkv(args, w):
             stream.wait_event(e_qkv)
             if out_free[bsel] is not None:
                 stream.wait_event(out_free[bsel])
-            dualkv.dualkv_fwd(qd, kd, vd, w.P, w.N, w.offsets, Hq, Hkv, D, w.scale, w.window, od, ld, stream)
+            run_fwd(qd, kd, vd, od, ld)
             e_fwd = torch.cuda.Event()
             e_fwd.record(stream)
             stream.wait_event(e_do)
-            dualkv.dualkv_bwd(qd, kd, vd, od, ld, dod, w.P, w.N, w.offsets, Hq, Hkv, D, w.scale, w.window, dqd, dkd,
-                              dvd, ws, None, stream)
+            run_bwd(qd, kd, vd, od, ld, dod, dqd, dkd, dvd)
             e_bwd = torch.cuda.Event()
             e_bwd.record(stream)
             in_free[bsel] = e_bwd
@@ -503,7 +542,8 @@ def run_dualkv(args, w):
         torch.cuda.synchronize(dev)
         ms_e2e = max_over_ranks(timed_e2e(max(2, min(args.steps, 10))), world, dev)
         dualkv.dualkv_check_status(stream)
-        e2e = {"value": world * f_step / (ms_e2e * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        job_flops = f_step if shard else world * f_step
+        e2e = {"value": job_flops / (ms_e2e * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e,
                "pipelining": "double-buffered device inputs/outputs; uploads and downloads on their own streams"}
         dins.clear()
@@ -511,7 +551,7 @@ def run_dualkv(args, w):
 
     # the same kernels on the replicated layout (prompt copied into every sequence)
     replicated = None
-    if not args.no_replicated:
+    if not args.no_replicated and not shard:
         wr = w.replicated()
         del out, dq
         torch.cuda.empty_cache()
@@ -553,15 +593,16 @@ def run_dualkv(args, w):
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "strong" if shard else "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "P": w.P, "N": w.N, "R": (w.R[0] if len(set(w.R)) == 1 else "ragged"),
                        "Hq": Hq, "Hkv": Hkv, "D": D, "window": w.window, "packed_tokens": T,
                        "replicated_tokens": w.T_replicated, "pairs_per_head": pairs,
                        "l2": "no flush: inputs larger than L2 (q+k+v+dO = %.2f GB)" % (
                            sum(x.numel() * x.element_size() for x in (q, k, v, do)) / 1e9),
-                       "parallelism": f"replicas x{world}"},
-            "pct_bf16_peak": {"measured_burst": value / world / pk["bf16_burst"],
+                       "parallelism": (f"kv-head groups x{world}" if shard else f"replicas x{world}")},
+            "pct_bf16_peak": {"measured_burst": value / world / pk["bf16_burst"],  # per GPU
                               "measured_sustained": value / world / pk["bf16_sustained"],
                               "nominal_2250": value / world / 2250.0},
             "fwd": {"ms": ms_fwd, "tflops": f_fwd / (ms_fwd * 1e-3) / 1e12},
@@ -690,6 +731,9 @@ def main(argv=None):
     ap.add_argument("--no-replicated", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pack", action="store_true", help="skip the pack/unpack/fold measurement")
+    ap.add_argument("--shard", choices=("replicas", "heads"), default="replicas",
+                    help="N > 1: independent replicas (weak scaling) or one micro-batch split by kv-head group "
+                         "(strong scaling)")
     ap.add_argument("--layers", default=None,
                     help="time a layer stack instead: a pattern of S (sliding) and G (global) layers, e.g. SSSSSG")
     ap.add_argument("--slide-window", type=int, default=1024, help="window of the S layers of --layers")

@@ -241,6 +241,21 @@ def dualkv_bwd_layers(qs, ks, vs, outs, lses, douts, windows, P, N, R_offsets, H
     _raise(rc, "dualkv_bwd_layers")
 
 
+def kv_head_ranges(Hkv: int, parts: int):
+    """Contiguous kv-head groups [lo, hi) for `parts` ranks (sizes differ by at most one;
+    a rank gets an empty range when parts > Hkv)."""
+    Hkv, parts = int(Hkv), int(parts)
+    if Hkv < 1 or parts < 1:
+        raise ValueError("Hkv and parts must be positive")
+    base, extra = divmod(Hkv, parts)
+    out, lo = [], 0
+    for r in range(parts):
+        hi = lo + base + (1 if r < extra else 0)
+        out.append((lo, hi))
+        lo = hi
+    return out
+
+
 def dualkv_bwd_noalloc(q, k, v, out, lse, dout, P, N, R_offsets, Hq, Hkv, D, scale, window, dq, dk, dv,
                        stream=None) -> None:
     """dualkv_bwd without a workspace: for callers that cannot allocate device

@@ -49,3 +49,84 @@ def test_aggregate_single_rank():
     import bench
     ms, value = bench.aggregate(8.0, 2e12, 1, torch.device("cpu"))
     assert ms == 8.0 and value == pytest.approx(250.0)
+
+
+# ---------------------------------------------------------------- head sharding (strong scaling)
+def test_kv_head_ranges_partition():
+    from shared_prompt_exact_gb300.dualkv import kv_head_ranges
+    for hkv in (1, 2, 3, 8):
+        for parts in (1, 2, 3, 4, 8, 9):
+            rs = kv_head_ranges(hkv, parts)
+            assert len(rs) == parts and rs[0][0] == 0 and rs[-1][1] == hkv
+            assert all(a[1] == b[0] for a, b in zip(rs, rs[1:]))
+            sizes = [hi - lo for lo, hi in rs]
+            assert max(sizes) - min(sizes) <= 1 and min(sizes) >= 0
+    with pytest.raises(ValueError):
+        kv_head_ranges(0, 2)
+
+
+def _strong_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    ms_local, flops_local = [(10.0, 3e12), (12.0, 1e12)][rank]
+    q.put((rank,) + bench.aggregate_strong(ms_local, flops_local, world, torch.device("cpu")))
+    dist.destroy_process_group()
+
+
+def test_aggregate_strong_two_ranks_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_strong_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    for rank, ms, value in sorted(q.get(timeout=10) for _ in range(2)):
+        assert ms == pytest.approx(12.0)
+        assert value == pytest.approx(4e12 / 12e-3 / 1e12)
+
+
+def _oracle_shard_worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import oracle
+    from shared_prompt_exact_gb300 import workloads as wl
+    from shared_prompt_exact_gb300.dualkv import kv_head_ranges
+    w = wl.custom(40, [17, 0, 30], 6, 3, 64, 0, seed=99)
+    qx, kx, vx, dox = wl.draw_inputs(w)
+    gs = w.Hq // w.Hkv
+    lo, hi = kv_head_ranges(w.Hkv, world)[rank]
+    part = oracle.dualkv(w.P, w.N, w.offsets, (hi - lo) * gs, hi - lo, w.D, w.scale, w.window,
+                         qx[:, lo * gs:hi * gs].contiguous(), kx[:, lo:hi].contiguous(), vx[:, lo:hi].contiguous(),
+                         dox[:, lo * gs:hi * gs].contiguous())
+    parts = [None] * world
+    dist.all_gather_object(parts, {k: part[k] for k in ("out", "lse", "dq", "dk", "dv")})
+    ok = True
+    if rank == 0:
+        import numpy as np
+        full = oracle.dualkv(w.P, w.N, w.offsets, w.Hq, w.Hkv, w.D, w.scale, w.window, qx, kx, vx, dox)
+        ok = (np.array_equal(np.concatenate([p["out"] for p in parts], axis=1), full["out"]) and
+              np.array_equal(np.concatenate([p["lse"] for p in parts], axis=0), full["lse"]) and
+              np.array_equal(np.concatenate([p["dq"] for p in parts], axis=1), full["dq"]) and
+              np.array_equal(np.concatenate([p["dk"] for p in parts], axis=1), full["dk"]) and
+              np.array_equal(np.concatenate([p["dv"] for p in parts], axis=1), full["dv"]))
+    q.put((rank, ok))
+    dist.destroy_process_group()
+
+
+def test_head_sharded_oracle_matches_full_gloo():
+    """Two ranks, each with a contiguous kv-head group (the split bench.py --shard heads
+    uses), reproduce the full result exactly: heads never interact."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_oracle_shard_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=300)
+        assert p.exitcode == 0
+    assert all(ok for _, ok in (q.get(timeout=10) for _ in range(2)))
