@@ -93,12 +93,13 @@ __device__ __forceinline__ uint32_t packed_kstep_col(int k) { return 32u * (k >>
 // ---------------------------------------------------------------- dQ
 // 128-key tiles: S and dP are M=128 x N=128 MMAs.  S and dP each have one TMEM
 // buffer, released as soon as the compute warps have loaded them, so the next
-// tile's S and dP run while the compute warps work.  dS goes to its own
-// double buffer (nothing the tensor pipe writes aliases what it reads).  NG
-// compute warps share each TMEM lane quarter; each thread handles BN / NG key
-// columns of its query row (two warps per quarter measured fastest: four were
-// slower).
-// TMEM: S 128 | dP 128 | dS 2 x 64 | dQ D columns.
+// tile's S and dP run while the compute warps work.  S = Q K^T takes Q from
+// TMEM (a TS MMA reads only K from shared memory; the SS form was bound by
+// shared-memory operand reads); the compute warps copy each item's Q tile there
+// from its TMA landing buffer.  dS goes to its own buffer, written once the
+// previous tile's dQ GEMM has completed.  NG compute warps share each TMEM lane
+// quarter; each thread handles BN / NG key columns of its query row (two warps
+// per quarter measured fastest: four were slower).
 // The kernel is persistent: CTA c takes work items c, c + grid, c + 2 grid, ...
 // of the cost-sorted list, and the pipeline runs on across items (ring slots
 // and barrier phases follow a tile counter over all of the CTA's tiles), so
