@@ -52,7 +52,7 @@ extern "C" {
 #define DUALKV_ERR_WORKSPACE 3   /* workspace missing or smaller than dualkv_bwd_workspace_bytes() */
 #define DUALKV_ERR_CUDA 4        /* a CUDA runtime call or kernel launch failed */
 #define DUALKV_ERR_DEVICE 5      /* a kernel reported a timeout or bounds violation */
-#define DUALKV_ERR_UNSUPPORTED 6 /* valid arguments outside what this build supports */
+#define DUALKV_ERR_UNSUPPORTED 6 /* valid arguments outside what this library supports */
 
 /*
  * Forward pass (paper abstract: "fused CUDA forward ... kernels that iterate

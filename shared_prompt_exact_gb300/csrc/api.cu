@@ -596,7 +596,7 @@ const char* dualkv_error_string(int code) {
     case DUALKV_ERR_DEVICE:
       return "a kernel reported a timed-out wait or an index out of range";
     case DUALKV_ERR_UNSUPPORTED:
-      return "valid arguments outside what this build supports";
+      return "valid arguments outside what this library supports";
     default:
       return "unknown error code";
   }
