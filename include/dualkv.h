@@ -5,10 +5,10 @@
  * Source of the method: "DualKV: Shared-Prompt Flash Attention for Efficient
  * RL Training with Large Rollouts and Long Contexts", abstract.  A micro-batch
  * holds one shared prompt of P tokens and N response segments; the data
- * pipeline packs the N(P+R) replicated tokens into P + sum_n R_n rows, and
- * the fused forward and backward kernels walk two disjoint KV regions (the
- * shared prompt and the query's own segment) in one launch.  The result is
- * stated to equal standard causal attention on the N replicated sequences.
+ * pipeline stores the N(P+R) replicated tokens as P + sum_n R_n rows, and
+ * each kernel walks, for a query, the prompt's keys and then those of the
+ * query's own segment within one launch.  By the paper's account the result
+ * is exactly causal attention on the N replicated sequences.
  *
  * Packed layout (all buffers contiguous, device memory unless stated):
  *   row t in [0, P)                 prompt token t, position t
@@ -55,9 +55,9 @@ extern "C" {
 #define DUALKV_ERR_UNSUPPORTED 6 /* valid arguments outside what this library supports */
 
 /*
- * Forward pass (paper abstract: "fused CUDA forward ... kernels that iterate
- * over two disjoint KV regions -- shared context and per-sequence response --
- * in a single kernel launch").  For every packed query row and q-head:
+ * Forward pass (paper abstract: one kernel launch covers both key ranges of a
+ * query, the shared prompt and the query's own response).  For every packed
+ * query row and q-head:
  * S = scale * q k^T over the allowed keys of the prompt region and then of the
  * row's own segment, online softmax, out = softmax(S) v, lse = log-sum-exp(S).
  *
@@ -158,7 +158,7 @@ int dualkv_bwd_layers(int n_layers, const void* const* q, const void* const* k, 
 
 /*
  * Packing indices (host only, no GPU needed; paper abstract: the pipeline
- * "repacks N(P+R) tokens into P+NR tokens").  All outputs are HOST int32:
+ * stores N(P+R) replicated tokens as P+NR rows).  All outputs are HOST int32:
  *   seg_id[T]          -1 for prompt rows, else the segment of the row
  *   pos_id[T]          position of the row in its replicated sequence
  *   cu_seqlens_rep[N+1] start of replicated sequence n (length P + R_n)
@@ -170,9 +170,9 @@ int dualkv_build_index(int P, int N, const int32_t* R_offsets, int32_t* seg_id, 
 
 /*
  * Per-token tensors between the replicated and the packed layout (paper
- * abstract: the pipeline repacks the N(P+R) tokens into P+NR, which extends the
- * token reduction from attention to the whole model; these calls move the
- * activations and gradients of the layers around attention).
+ * abstract: with the prompt stored once, the layers around attention also run
+ * on P+NR rows; these calls move their activations and gradients between the
+ * two layouts).
  *
  * Replicated layout: sequence n is the P prompt rows followed by its R_n
  * response rows; the sequences lie end to end (sequence n starts at row

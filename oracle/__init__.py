@@ -9,7 +9,8 @@ Contents
 * ``dualkv_oracle.c`` (loaded here through ctypes): the plain definition --
   standard causal attention on the N replicated sequences, its analytic
   backward, and the fold of replicated prompt gradients by summation
-  (DualKV paper, abstract: "mathematically equivalent to standard attention").
+  (DualKV paper, abstract: the packed result is exactly that of ordinary
+  attention on the replicated sequences).
 * ``brute``: an independent dense numpy formulation over the *packed* rows with
   an explicit T x T mask, used to pin the C oracle on tiny inputs.
 * ``index``: an independent pure-Python packing-index builder (seg-id, pos-id,

@@ -12,7 +12,7 @@
  *
  *   1. Unpack the packed micro-batch [prompt P][seg 0 R_0]...[seg N-1] into N
  *      replicated sequences X_n = prompt rows ++ segment-n rows, positions
- *      0..P+R_n-1 (the abstract's "N(P+R) tokens").
+ *      0..P+R_n-1 (the N(P+R) replicated tokens of the abstract).
  *   2. Per replica, per q-head h (kv-head g = h / (Hq/Hkv)), per row i:
  *      allowed keys A_i = { j <= i : window <= 0 or i - j < window },
  *      S_ij = scale * q_i . k_j,  m_i = max_j S_ij,  l_i = sum_j exp(S_ij - m_i),

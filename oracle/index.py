@@ -1,7 +1,8 @@
 """Packing-index oracle -- TEST INFRASTRUCTURE (see ``oracle/__init__``).
 
 Plain Python restatement of the packed micro-batch layout of DualKV (paper
-abstract: the data pipeline "repacks N(P+R) tokens into P+NR tokens"):
+abstract: the data pipeline stores the N(P+R) tokens of N replicated sequences
+as P+NR rows, the prompt only once):
 packed rows are [prompt 0..P-1][segment 0][segment 1]...[segment N-1], where
 segment n holds rows P+off[n] .. P+off[n+1]-1.  The replicated layout is the
 N sequences prompt ++ segment n laid end to end.

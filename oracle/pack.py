@@ -3,8 +3,9 @@
 Plain numpy definitions of the three tensor-level moves between the
 replicated and the packed micro-batch layout.  They carry the token reduction
 of shared-prompt packing past attention: per-token layers then run on P+NR
-rows instead of N(P+R) (DualKV paper, abstract: the repacking "extends the
-token reduction from attention to the entire model").
+rows instead of N(P+R) (DualKV paper, abstract: once the data pipeline stores
+the prompt once, every per-token layer of the model, not only attention,
+works on the smaller row count).
 
 All three are written through ``rep2pack`` of ``oracle.index`` (the packed row
 of every replicated row):

@@ -2,7 +2,8 @@
 //
 // The packed backward equals the analytic backward of standard attention on
 // the N replicated sequences with the prompt gradients summed over replicas
-// (DualKV paper, abstract: mathematically equivalent to standard attention).
+// (DualKV paper, abstract: packing changes nothing in the result, which is
+// exactly that of ordinary attention on the replicated sequences).
 // With P_ij = exp(S_ij - LSE_i), dP_ij = dO_i . v_j, Delta_i = dO_i . O_i and
 // dS_ij = P_ij (dP_ij - Delta_i):
 //   dQ_i = scale sum_j dS_ij k_j,   dK_j = scale sum_i dS_ij q_i,   dV_j = sum_i P_ij dO_i.

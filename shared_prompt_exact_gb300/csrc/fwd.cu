@@ -1,8 +1,8 @@
 // fwd.cu -- DualKV forward kernel for sm_103a (head dimension 64, 128, 512).
 //
-// DualKV paper, abstract: a fused forward kernel that iterates over two
-// disjoint KV regions -- the shared prompt and the query's own response
-// segment -- in a single launch.  One CTA takes one query tile (128 packed
+// DualKV paper, abstract: the keys a packed query sees lie in two separate
+// ranges of rows, the prompt that all segments share and the query's own
+// segment, and one kernel covers both in the same launch.  One CTA takes one query tile (128 packed
 // rows of one region) of one q-head and walks the key tiles of region 0
 // (prompt) and then region 1 (own segment), clipped to the causal / window
 // range, with an online softmax.

@@ -1,7 +1,7 @@
 // pack.cu -- moving per-token tensors between the replicated and the packed
 // layout, so that the token reduction of shared-prompt packing reaches the
-// layers around attention (DualKV paper, abstract: extending the reduction
-// from attention to the whole model).
+// layers around attention (DualKV paper, abstract: with the prompt stored
+// once, every per-token layer, not only attention, works on fewer rows).
 //
 //   replicated: sequence n = prompt rows 0..P-1 then its R_n response rows,
 //               sequences laid end to end; sequence n starts at n*P + off[n]

@@ -1,7 +1,7 @@
 """Pins of the fp64 oracle against things other than itself.
 
-DualKV paper, abstract: DualKV is "mathematically equivalent to standard
-attention".  The oracle writes that definition out (replicated causal
+DualKV paper, abstract: the packed computation gives exactly what ordinary
+attention gives on the replicated sequences.  The oracle writes that definition out (replicated causal
 attention + analytic backward + fold).  These tests tie it to:
   * an independent dense packed-mask formulation (oracle.brute);
   * torch float64 autograd through the library's scaled_dot_product_attention
