@@ -130,3 +130,26 @@ def test_head_sharded_oracle_matches_full_gloo():
         p.join(timeout=300)
         assert p.exitcode == 0
     assert all(ok for _, ok in (q.get(timeout=10) for _ in range(2)))
+
+
+def test_reference_arm_json_line():
+    """bench.py --impl reference prints one JSON line with the contract's keys (CPU only:
+    the reference arm times the fp64 oracle on the host cores)."""
+    import contextlib
+    import io
+    import json
+    import bench
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        rc = bench.main(["--impl", "reference", "--config", "tiny", "--steps", "2", "--warmup", "1"])
+    assert rc == 0
+    lines = [ln for ln in buf.getvalue().splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "TFLOP/s"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"] == "tiny"
