@@ -5,6 +5,7 @@ statically so the library needs only the NVIDIA driver at run time.
 """
 from __future__ import annotations
 
+import fcntl
 import os
 import subprocess
 import sys
@@ -37,10 +38,24 @@ def _newest_input() -> float:
     return max(t, os.path.getmtime(__file__))
 
 
+def _up_to_date() -> bool:
+    return os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= _newest_input()
+
+
 def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= _newest_input():
+    if not force and _up_to_date():
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
+    # one build at a time (ranks of a multi-process launch may all call this);
+    # a process that waited finds the library up to date
+    with open(os.path.join(BUILD_DIR, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and _up_to_date():
+            return LIB_PATH
+        return _build_locked(verbose, extra_flags)
+
+
+def _build_locked(verbose: bool, extra_flags) -> str:
     nvcc = _nvcc()
     flags = NVCC_FLAGS + list(extra_flags or [])
 
