@@ -110,3 +110,50 @@ def test_binding_refuses_cpu_tensors(lib):
 def test_selftest_rejects_out_of_range_limit(lib):
     assert lib.dualkv_selftest_timeout(10, None) == dualkv.DUALKV_ERR_INVALID
     assert lib.dualkv_selftest_timeout(100 * 10**9, None) == dualkv.DUALKV_ERR_INVALID
+
+
+def test_head_range_validation_before_any_device_work(lib):
+    off = (ctypes.c_int32 * 2)(0, 2)
+    p, bad = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x10008)
+    # kv-head range must satisfy 0 <= begin < end <= Hkv
+    for lo, hi in ((1, 1), (-1, 1), (0, 3), (2, 1)):
+        assert lib.dualkv_fwd_heads(p, p, p, 4, 1, off, 4, 2, 128, 0.125, 0, lo, hi, p, p, None) == \
+            dualkv.DUALKV_ERR_INVALID
+        assert lib.dualkv_bwd_heads(p, p, p, p, p, p, 4, 1, off, 4, 2, 128, 0.125, 0, lo, hi, p, p, p, p, 1 << 20,
+                                    None) == dualkv.DUALKV_ERR_INVALID
+    assert lib.dualkv_fwd_heads(p, p, p, 4, 1, off, 4, 2, 128, 0.125, 0, 0, 1, bad, p, None) == dualkv.DUALKV_ERR_ALIGN
+
+
+def test_layer_stack_validation_before_any_device_work(lib):
+    off = (ctypes.c_int32 * 2)(0, 2)
+    n = 2
+    good = (ctypes.c_void_p * n)(0x10000, 0x20000)
+    mixed = (ctypes.c_void_p * n)(0x10000, 0x20008)  # the second layer's pointer is misaligned
+    win = (ctypes.c_int32 * n)(0, 64)
+    assert lib.dualkv_fwd_layers(0, good, good, good, win, 4, 1, off, 4, 2, 128, 0.125, good, good, None) == \
+        dualkv.DUALKV_ERR_INVALID
+    assert lib.dualkv_fwd_layers(n, None, good, good, win, 4, 1, off, 4, 2, 128, 0.125, good, good, None) == \
+        dualkv.DUALKV_ERR_INVALID
+    assert lib.dualkv_fwd_layers(n, good, good, good, win, 4, 1, off, 4, 3, 128, 0.125, good, good, None) == \
+        dualkv.DUALKV_ERR_INVALID
+    assert lib.dualkv_fwd_layers(n, good, good, mixed, win, 4, 1, off, 4, 2, 128, 0.125, good, good, None) == \
+        dualkv.DUALKV_ERR_ALIGN
+    assert lib.dualkv_bwd_layers_workspace_bytes(0, win, 4, 1, off, 4, 2, 128) == 0
+    assert lib.dualkv_bwd_layers_workspace_bytes(n, None, 4, 1, off, 4, 2, 128) == 0
+    # the stack needs what its most demanding window needs
+    single = [lib.dualkv_bwd_workspace_bytes(4, 1, off, 4, 2, 128, w) for w in (0, 64)]
+    assert lib.dualkv_bwd_layers_workspace_bytes(n, win, 4, 1, off, 4, 2, 128) == max(single) > 0
+
+
+def test_pack_validation_before_any_device_work(lib):
+    off = (ctypes.c_int32 * 3)(0, 2, 3)   # P = 4, N = 2: T = 7, T_rep = 11 rows
+    src, dst = ctypes.c_void_p(0x100000), ctypes.c_void_p(0x200000)
+    assert lib.dualkv_pack(src, dst, 4, 2, off, 12, None) == dualkv.DUALKV_ERR_INVALID    # not whole 16-byte vectors
+    assert lib.dualkv_pack(src, dst, 4, 2, off, 0, None) == dualkv.DUALKV_ERR_INVALID
+    assert lib.dualkv_pack(src, dst, -1, 2, off, 16, None) == dualkv.DUALKV_ERR_INVALID
+    assert lib.dualkv_unpack(src, None, 4, 2, off, 16, None) == dualkv.DUALKV_ERR_INVALID
+    # source and destination ranges overlap (11 replicated rows of 32 bytes from 0x100000)
+    assert lib.dualkv_fold(src, ctypes.c_void_p(0x100000 + 5 * 32), 4, 2, off, 16, None) == dualkv.DUALKV_ERR_INVALID
+    assert lib.dualkv_pack(ctypes.c_void_p(0x100008), dst, 4, 2, off, 16, None) == dualkv.DUALKV_ERR_ALIGN
+    bad_off = (ctypes.c_int32 * 3)(0, 3, 2)
+    assert lib.dualkv_pack(src, dst, 4, 2, bad_off, 16, None) == dualkv.DUALKV_ERR_INVALID
