@@ -440,6 +440,10 @@ int oracle_key_rows(int P, int N, const int32_t *off, int Hq, int Hkv, int D, do
         for (int r = 0; r < nkeys; ++r)
           if (kpos[r] >= j0 && kpos[r] <= i) sees = 1;
         if (!sees) continue;
+        /* Under the replica-0 split a prompt row of replica n >= 1 carries a zero
+           upstream gradient, so its dV term p * 0 and its dK term scale * p * (0 - 0) * q
+           are zeros: adding them changes no sum, and the row is skipped. */
+        if (dout_mode == 0 && n > 0 && i < P) continue;
         double m, l;
         forward_row(&L, n, h, i, q, k, v, oi, &m, &l, sbuf);
         replica_dout(&L, n, h, i, dout, dout_mode, doi);

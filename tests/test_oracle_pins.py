@@ -288,6 +288,19 @@ def test_sampled_rows_match_full_oracle():
         assert np.max(np.abs(dv - o["dv"][keys, g])) <= 1e-12
 
 
+def test_sampled_prompt_keys_match_full_oracle_under_both_dout_splits():
+    # key_rows skips the prompt rows of replicas >= 1 when only replica 0 carries the
+    # prompt's upstream gradient; both splits must give the full oracle's folded dK/dV
+    c = rand_case(21, 10, [6, 3, 0, 8], 4, 1, 8, 0)
+    keys = [0, 1, 5, 9, 10, 17, 26]
+    for mode in (0, 1):
+        o = run_oracle(c, dout_mode=mode)
+        dk, dv = oracle.key_rows(c["P"], c["N"], c["off"], 4, 1, 8, c["scale"], 0, 0, keys,
+                                 c["q"], c["k"], c["v"], c["do"], dout_mode=mode)
+        assert np.max(np.abs(dk - o["dk"][keys, 0])) <= 1e-12
+        assert np.max(np.abs(dv - o["dv"][keys, 0])) <= 1e-12
+
+
 def test_index_oracle_small_layout():
     seg, pos, cu, r2p = oindex.build_index(3, [0, 2, 2, 3])
     assert seg == [-1, -1, -1, 0, 0, 2]
@@ -307,3 +320,26 @@ def test_pairs_closed_form():
         assert oindex.pairs(P, off) == int(brute.packed_mask(P, off).sum())
     off = [0, 4, 9]
     assert oindex.pairs(6, off, window=3) == int(brute.packed_mask(6, off, 3).sum())
+
+
+def test_pairs_replicated_counts_the_replicated_mask():
+    # the replicated layout is N independent sequences of P + R_n tokens, i.e. a
+    # packed layout with no prompt whose segments are those sequences; its pair
+    # count is that mask's population and, for global causal attention, the sum of
+    # the sequences' triangles L_n (L_n + 1) / 2
+    for P, R, W in ((5, [3, 0, 4], 0), (0, [2, 2], 0), (7, [1], 0), (6, [4, 5], 3), (4, [0, 6, 2], 1),
+                    (9, [3, 3], 100)):
+        off = [0]
+        for r in R:
+            off.append(off[-1] + r)
+        rep_off = [0]
+        for r in R:
+            rep_off.append(rep_off[-1] + P + r)
+        got = oindex.pairs_replicated(P, off, W)
+        assert got == int(brute.packed_mask(0, rep_off, W).sum())
+        if W <= 0:
+            assert got == sum((P + r) * (P + r + 1) // 2 for r in R)
+        # replicating never removes a pair: every packed pair appears at least once
+        assert got >= oindex.pairs(P, off, W)
+        if len(R) == 1:
+            assert got == oindex.pairs(P, off, W)
