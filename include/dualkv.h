@@ -27,14 +27,16 @@
  * accumulated.  Results are bitwise deterministic for a given GPU, library
  * build and input.  Inputs must be finite.  Every device pointer must be
  * 16-byte aligned.  The caller owns every buffer it passes; the library owns
- * only a per-layout plan cache (small device arrays) and a per-device status
- * word, both freed by dualkv_release().
+ * only a bounded per-layout plan cache (small device arrays, see
+ * dualkv_plan_cache_info) and a per-device status word, both freed by
+ * dualkv_release().
  *
  * Return codes: DUALKV_OK, or one of the DUALKV_ERR_* values below; on an
- * error nothing is launched (except DUALKV_ERR_CUDA, which reports a failed
- * launch).  Kernel-side failures (a bounded wait that timed out, an index
- * out of range) do not abort the launch: they are recorded in the status
- * word and reported by dualkv_check_status().
+ * error no kernel is launched (except DUALKV_ERR_CUDA, which reports a failed
+ * launch).  Kernel-side failures do not abort the launch: a bounded wait that
+ * timed out, or a work-list entry whose rows fall outside the tensors (the
+ * kernels check each entry before using it and skip it), is recorded in the
+ * status word and reported by dualkv_check_status().
  */
 #ifndef DUALKV_H_
 #define DUALKV_H_
@@ -252,20 +254,23 @@ int dualkv_profile_read(double* ms, int64_t* launches);
  * own pool at start-up and fails any later allocation, or a host binding that
  * owns no device allocator and holds only the buffers it was given.
  *
- * Same arguments and results as dualkv_bwd, without the workspace: Delta,
- * the log2-scaled LSE, the split dK/dV partials, the work lists and a status
- * word live in one fixed array of DUALKV_NOALLOC_SCRATCH_BYTES (32 MiB) in
- * the library's device memory, which every GPU that loads the library holds
- * until the process exits.  The first call on a device looks up that array's
- * device address (set-up), so make that first call before any stream capture
- * on the device.  A layout whose scratch would exceed the maximum is rejected
- * with DUALKV_ERR_WORKSPACE before anything is launched.  Every call shares
- * the array and leaves its contents behind; the status word is cleared at the
+ * Same arguments and results as dualkv_bwd for head dimensions 64 and 128,
+ * without the workspace; D = 512 returns DUALKV_ERR_UNSUPPORTED (its bf16 P and
+ * dS blocks need gigabytes, far beyond a fixed array).  Delta, the log2-scaled
+ * LSE, the split dK/dV partials, the work lists and a status word live in one
+ * fixed array of DUALKV_NOALLOC_SCRATCH_BYTES (32 MiB) in the library's device
+ * memory, which every GPU that loads the library holds until the process
+ * exits.  The first call on a device looks up that array's device address
+ * (set-up), so make that first call before any stream capture on the device.
+ * A layout whose scratch would exceed the maximum is rejected with
+ * DUALKV_ERR_WORKSPACE before anything is launched.  Every call shares the
+ * array and leaves its contents behind; the status word is cleared at the
  * start of each call and everything else is fully written before it is read.
  * Calls that overlap on the GPU (different streams, or host threads) race on
- * the array and corrupt each other's results.  The call returns after its
- * kernels have finished on `stream`, with DUALKV_ERR_DEVICE if one of them
- * reported a timed-out wait or an index out of range.
+ * the array and corrupt each other's results.  The call is synchronous: it
+ * returns after its kernels have finished on `stream` (also when it fails
+ * after queueing work), with DUALKV_ERR_DEVICE if one of them reported a
+ * timed-out wait or an index out of range.
  */
 #define DUALKV_NOALLOC_SCRATCH_BYTES 33554432
 int dualkv_bwd_noalloc(const void* q, const void* k, const void* v, const void* out, const float* lse,
@@ -284,6 +289,39 @@ int dualkv_bwd_noalloc(const void* q, const void* k, const void* v, const void* 
  * fails, else DUALKV_OK.
  */
 int dualkv_selftest_timeout(uint64_t limit_ns, void* stream);
+
+/*
+ * Self-test of the production kernels' failure paths (no counterpart in the
+ * paper; it exists so that timeout and range handling can be tested without
+ * faulting a GPU).  Runs one kernel on a tiny internal layout (zero inputs,
+ * P = 128, two responses of 128, one head, D = 128) with every bounded wait
+ * limited to limit_ns nanoseconds (1 ms .. 10 s):
+ *   which = 0  the forward kernel; the first K/V tile of every CTA is never
+ *              loaded, so the wait for it runs out;
+ *   which = 1  the dK/dV kernel; the first query block of its first CTA gets
+ *              one barrier arrival too few, so the waits for it run out;
+ *   which = 2  the forward kernel given a work list whose first entry lies past
+ *              the last row; the kernel's range check skips it.
+ * Each kernel records the failure in the status word, drains its copies and
+ * tensor-core operations, frees its tensor memory and returns;
+ * dualkv_check_status() then reports DUALKV_ERR_DEVICE and the context stays
+ * usable.  The call allocates and frees its own small buffers and returns
+ * after the kernel has finished on `stream`: DUALKV_OK, DUALKV_ERR_INVALID
+ * (which or limit out of range) or DUALKV_ERR_CUDA.
+ */
+int dualkv_selftest_kernel(int which, uint64_t limit_ns, void* stream);
+
+/*
+ * The library keeps the work lists of the 32 most recently used layouts
+ * (per layout, window, head dimension and kv-head range) in device memory and
+ * evicts the least recently used one beyond that; the memory of evicted plans
+ * is pooled and reused, so a training loop whose offsets change every
+ * micro-batch neither grows device memory nor allocates on every call.  Plans
+ * are uploaded with one asynchronous copy on the caller's stream.  Reports the
+ * number of resident plans and the device bytes the cache holds (resident and
+ * pooled); either pointer may be NULL.  Returns DUALKV_OK.
+ */
+int dualkv_plan_cache_info(int* n_plans, int64_t* device_bytes);
 
 /* Frees the plan cache, status words and timing events.  Not safe while launches are pending. */
 void dualkv_release(void);

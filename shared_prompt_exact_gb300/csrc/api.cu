@@ -15,6 +15,7 @@
 #include "../../include/dualkv.h"
 #include "kernels.h"
 #include "plan.h"
+#include "plan_cache.h"
 
 using namespace dkv;
 
@@ -32,9 +33,99 @@ std::map<int, uint32_t*> g_status;  // device -> status word
 // split into contiguous chunks reduced in a fixed order.
 constexpr int kMaxDkvIters = 512;
 
+// ---------------------------------------------------------------- plan cache
+// Device memory of the plans comes from "blobs": one device buffer plus one
+// pinned host buffer of the same capacity.  A plan's arrays are serialised
+// into the host buffer and uploaded with a single cudaMemcpyAsync on the
+// caller's stream (no synchronisation); an event recorded after the copy
+// (`ready`) lets calls on other streams wait for it, and an event recorded
+// after the last launch that read the plan (`last_use`) tells when its blob may
+// be reused.  Evicted plans return their blobs to a small per-process pool, so
+// a loop whose layout changes every call reuses the same few buffers instead
+// of allocating.
+struct Blob {
+  int device = -1;
+  void* d = nullptr;  // device
+  void* h = nullptr;  // pinned host
+  size_t cap = 0;
+};
+
+constexpr size_t kPlanCacheCapacity = 32;   // layouts whose plans stay resident
+constexpr size_t kFreeBlobsKept = 16;       // released blobs kept for reuse
+
+std::vector<Blob> g_free_blobs;
+size_t g_blob_bytes = 0;  // device bytes held by all blobs (in use or pooled)
+
+void free_blob(Blob& b) {
+  if (b.d) cudaFree(b.d);
+  if (b.h) cudaFreeHost(b.h);
+  g_blob_bytes -= b.cap;
+  b = Blob{};
+}
+
+// A blob of at least `bytes` on `device`: the smallest pooled one that fits, else a new one.
+int acquire_blob(int device, size_t bytes, Blob* out) {
+  size_t best = g_free_blobs.size();
+  for (size_t i = 0; i < g_free_blobs.size(); ++i)
+    if (g_free_blobs[i].device == device && g_free_blobs[i].cap >= bytes &&
+        (best == g_free_blobs.size() || g_free_blobs[i].cap < g_free_blobs[best].cap))
+      best = i;
+  if (best < g_free_blobs.size()) {
+    *out = g_free_blobs[best];
+    g_free_blobs.erase(g_free_blobs.begin() + best);
+    return DUALKV_OK;
+  }
+  Blob b;
+  b.device = device;
+  b.cap = ((bytes + bytes / 4) + 65535) & ~size_t(65535);  // headroom so later layouts fit
+  if (cudaMalloc(&b.d, b.cap) != cudaSuccess) return DUALKV_ERR_CUDA;
+  if (cudaMallocHost(&b.h, b.cap) != cudaSuccess) {
+    cudaFree(b.d);
+    return DUALKV_ERR_CUDA;
+  }
+  g_blob_bytes += b.cap;
+  *out = b;
+  return DUALKV_OK;
+}
+
+// Returns a blob whose last reader has finished to the pool; beyond kFreeBlobsKept
+// the smallest pooled blobs are freed (large ones fit any later plan).
+void release_blob(Blob& b) {
+  if (!b.d) return;
+  g_free_blobs.push_back(b);
+  b = Blob{};
+  while (g_free_blobs.size() > kFreeBlobsKept) {
+    size_t small = 0;
+    for (size_t i = 1; i < g_free_blobs.size(); ++i)
+      if (g_free_blobs[i].cap < g_free_blobs[small].cap) small = i;
+    free_blob(g_free_blobs[small]);
+    g_free_blobs.erase(g_free_blobs.begin() + small);
+  }
+}
+
+// Host-side serialisation of several arrays into one blob (16-byte aligned parts).
+struct Packer {
+  std::vector<uint8_t> bytes;
+  template <typename T>
+  size_t add(const std::vector<T>& v) {
+    const size_t off = (bytes.size() + 15) & ~size_t(15);
+    bytes.resize(off + sizeof(T) * v.size());
+    if (!v.empty()) std::memcpy(bytes.data() + off, v.data(), sizeof(T) * v.size());
+    return off;
+  }
+};
+
+// One plan part (forward, or backward) in device memory.
+struct PlanPart {
+  Blob blob;
+  cudaEvent_t ready = nullptr;  // recorded after the upload
+  bool built = false;
+};
+
 struct DevPlan {
   int device = -1;
-  bool fwd_ready = false, bwd_ready = false;
+  cudaEvent_t last_use = nullptr;  // recorded after the last launch that read the plan
+  PlanPart fwd, bwd;
   QTileItem* fwd_items = nullptr;
   int n_fwd = 0;
   QTileItem* dq_items = nullptr;
@@ -51,25 +142,50 @@ struct DevPlan {
   XTItem* xt_items = nullptr;
   int n_xt = 0;
   XTEntry* xt_entries = nullptr;
-  ~DevPlan() {
-    cudaFree(block_base);
-    cudaFree(xt_items);
-    cudaFree(xt_entries);
-    cudaFree(fwd_items);
-    cudaFree(dq_items);
-    cudaFree(kv_items);
-    cudaFree(qblocks);
-    cudaFree(reduces);
-  }
+  int64_t n_xt_entries = 0;
 };
-std::map<std::string, std::unique_ptr<DevPlan>> g_plans;
+
+// Waits until no launch reads the plan any more, then returns its memory to the pool.
+void retire_plan(DevPlan& pl) {
+  for (PlanPart* part : {&pl.fwd, &pl.bwd}) {
+    if (part->ready) {
+      cudaEventSynchronize(part->ready);
+      cudaEventDestroy(part->ready);
+      part->ready = nullptr;
+    }
+  }
+  if (pl.last_use) {
+    cudaEventSynchronize(pl.last_use);
+    cudaEventDestroy(pl.last_use);
+    pl.last_use = nullptr;
+  }
+  release_blob(pl.fwd.blob);
+  release_blob(pl.bwd.blob);
+}
+
+LruCache<DevPlan> g_plans(kPlanCacheCapacity);
 
 struct DevOffsets {
   int32_t* d = nullptr;
   int num_sms = 0;
-  ~DevOffsets() { cudaFree(d); }
+  PlanPart part;
+  cudaEvent_t last_use = nullptr;
 };
-std::map<std::string, std::unique_ptr<DevOffsets>> g_offsets;  // (device, P, N, R_offsets) -> device copy
+LruCache<DevOffsets> g_offsets(kPlanCacheCapacity);  // (device, P, N, R_offsets) -> device copy
+
+void retire_offsets(DevOffsets& o) {
+  if (o.part.ready) {
+    cudaEventSynchronize(o.part.ready);
+    cudaEventDestroy(o.part.ready);
+    o.part.ready = nullptr;
+  }
+  if (o.last_use) {
+    cudaEventSynchronize(o.last_use);
+    cudaEventDestroy(o.last_use);
+    o.last_use = nullptr;
+  }
+  release_blob(o.part.blob);
+}
 
 std::string plan_key(int device, int P, int N, const int32_t* off, int Hq, int Hkv, int D, int window, int kv_lo = 0,
                      int kv_hi = 0) {
@@ -81,13 +197,48 @@ std::string plan_key(int device, int P, int N, const int32_t* off, int Hq, int H
   return k;
 }
 
+// Serialised part -> pinned host buffer -> one asynchronous copy on `st`; records `ready`.
+int upload_part(int device, const Packer& pk, cudaStream_t st, PlanPart* part) {
+  const size_t bytes = pk.bytes.empty() ? 16 : pk.bytes.size();
+  int rc = acquire_blob(device, bytes, &part->blob);
+  if (rc) return rc;
+  if (!pk.bytes.empty()) {
+    std::memcpy(part->blob.h, pk.bytes.data(), pk.bytes.size());
+    if (cudaMemcpyAsync(part->blob.d, part->blob.h, pk.bytes.size(), cudaMemcpyHostToDevice, st) != cudaSuccess) {
+      cudaStreamSynchronize(st);  // the blob goes back to the pool: nothing may still copy into it
+      release_blob(part->blob);
+      return DUALKV_ERR_CUDA;
+    }
+  }
+  if (!part->ready && cudaEventCreateWithFlags(&part->ready, cudaEventDisableTiming) != cudaSuccess)
+    return DUALKV_ERR_CUDA;
+  if (cudaEventRecord(part->ready, st) != cudaSuccess) return DUALKV_ERR_CUDA;
+  part->built = true;
+  return DUALKV_OK;
+}
+
 template <typename T>
-cudaError_t upload(T** dst, const std::vector<T>& v) {
-  *dst = nullptr;
-  if (v.empty()) return cudaSuccess;
-  cudaError_t e = cudaMalloc(dst, sizeof(T) * v.size());
-  if (e != cudaSuccess) return e;
-  return cudaMemcpy(*dst, v.data(), sizeof(T) * v.size(), cudaMemcpyHostToDevice);
+T* at(const PlanPart& part, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(part.blob.d) + off);
+}
+
+// Orders `st` after the part's upload (a no-op once the copy has completed).
+int wait_part(const PlanPart& part, cudaStream_t st) {
+  if (part.ready && cudaStreamWaitEvent(st, part.ready, 0) != cudaSuccess) return DUALKV_ERR_CUDA;
+  return DUALKV_OK;
+}
+
+// Marks the end of the launches that read the plan on `st`.
+int mark_use(cudaEvent_t* ev, cudaStream_t st) {
+  if (!*ev && cudaEventCreateWithFlags(ev, cudaEventDisableTiming) != cudaSuccess) return DUALKV_ERR_CUDA;
+  return cudaEventRecord(*ev, st) == cudaSuccess ? DUALKV_OK : DUALKV_ERR_CUDA;
+}
+
+template <class V, class Retire>
+void insert_retiring(LruCache<V>& cache, const std::string& key, std::unique_ptr<V> v, Retire retire) {
+  std::vector<std::unique_ptr<V>> evicted;
+  cache.insert(key, std::move(v), &evicted);
+  for (auto& e : evicted) retire(*e);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -129,54 +280,66 @@ int make_tmap(CUtensorMap* m, const void* base, int64_t T, int H, int D, int box
   return r == CUDA_SUCCESS ? DUALKV_OK : DUALKV_ERR_CUDA;
 }
 
-// Looks up (or builds) the plan of a layout restricted to kv-heads [kv_lo, kv_hi);
-// caller holds g_mu.
+// Looks up (or builds and uploads on `st`) the plan of a layout restricted to kv-heads
+// [kv_lo, kv_hi), and orders `st` after its uploads; caller holds g_mu.
 int get_plan(int P, int N, const int32_t* off, int Hq, int Hkv, int D, int window, int kv_lo, int kv_hi,
-             bool need_bwd, DevPlan** out) {
+             bool need_bwd, cudaStream_t st, DevPlan** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DUALKV_ERR_CUDA;
   const std::string key = plan_key(dev, P, N, off, Hq, Hkv, D, window, kv_lo, kv_hi);
-  auto& slot = g_plans[key];
-  if (!slot) {
-    slot.reset(new DevPlan());
-    slot->device = dev;
+  DevPlan* pl = g_plans.find(key);
+  if (!pl) {
+    std::unique_ptr<DevPlan> fresh(new DevPlan());
+    fresh->device = dev;
+    pl = fresh.get();
+    insert_retiring(g_plans, key, std::move(fresh), retire_plan);
   }
-  DevPlan* pl = slot.get();
   Layout L{P, N, std::vector<int32_t>(off, off + N + 1), Hq, Hkv, D, window <= 0 ? 0 : window, kv_lo, kv_hi};
-  if (!pl->fwd_ready) {
+  int rc;
+  if (!pl->fwd.built) {
+    Packer pk;
     auto items = plan_qtiles(L, fwd_query_tile(D), fwd_key_tile(D));
-    if (upload(&pl->fwd_items, items) != cudaSuccess) return DUALKV_ERR_CUDA;
+    const size_t o_items = pk.add(items);
+    if ((rc = upload_part(dev, pk, st, &pl->fwd))) return rc;
+    pl->fwd_items = at<QTileItem>(pl->fwd, o_items);
     pl->n_fwd = (int)items.size();
-    pl->fwd_ready = true;
   }
-  if (need_bwd && !pl->bwd_ready && D == 512) {
-    auto dq = plan_qtiles(L, 128, 128);
-    if (upload(&pl->dq_items, dq) != cudaSuccess) return DUALKV_ERR_CUDA;
-    pl->n_dq = (int)dq.size();
-    Plan512 p5 = plan_512(L, dq, kMaxDkvIters);
-    if (upload(&pl->block_base, p5.block_base) != cudaSuccess) return DUALKV_ERR_CUDA;
-    if (upload(&pl->xt_items, p5.items) != cudaSuccess) return DUALKV_ERR_CUDA;
-    if (upload(&pl->xt_entries, p5.entries) != cudaSuccess) return DUALKV_ERR_CUDA;
-    if (upload(&pl->reduces, p5.reduces) != cudaSuccess) return DUALKV_ERR_CUDA;
-    pl->n_blocks = p5.n_blocks;
-    pl->n_xt = (int)p5.items.size();
-    pl->n_reduce = (int)p5.reduces.size();
-    pl->nslots = p5.nslots;
-    pl->bwd_ready = true;
+  if (need_bwd && !pl->bwd.built) {
+    Packer pk;
+    if (D == 512) {
+      auto dq = plan_qtiles(L, 128, 128);
+      Plan512 p5 = plan_512(L, dq, kMaxDkvIters);
+      const size_t o_dq = pk.add(dq), o_bb = pk.add(p5.block_base), o_xi = pk.add(p5.items),
+                   o_xe = pk.add(p5.entries), o_red = pk.add(p5.reduces);
+      if ((rc = upload_part(dev, pk, st, &pl->bwd))) return rc;
+      pl->dq_items = at<QTileItem>(pl->bwd, o_dq);
+      pl->n_dq = (int)dq.size();
+      pl->block_base = at<int32_t>(pl->bwd, o_bb);
+      pl->xt_items = at<XTItem>(pl->bwd, o_xi);
+      pl->xt_entries = at<XTEntry>(pl->bwd, o_xe);
+      pl->reduces = at<ReduceItem>(pl->bwd, o_red);
+      pl->n_blocks = p5.n_blocks;
+      pl->n_xt_entries = (int64_t)p5.entries.size();
+      pl->n_xt = (int)p5.items.size();
+      pl->n_reduce = (int)p5.reduces.size();
+      pl->nslots = p5.nslots;
+    } else {
+      auto dq = plan_qtiles(L, dq_query_tile(D), dq_key_tile(D));
+      KVPlan kv = plan_kvtiles(L, dkv_key_tile(D), dkv_query_block(D), kMaxDkvIters);
+      const size_t o_dq = pk.add(dq), o_kv = pk.add(kv.items), o_qb = pk.add(kv.qblocks), o_red = pk.add(kv.reduces);
+      if ((rc = upload_part(dev, pk, st, &pl->bwd))) return rc;
+      pl->dq_items = at<QTileItem>(pl->bwd, o_dq);
+      pl->n_dq = (int)dq.size();
+      pl->kv_items = at<KVTileItem>(pl->bwd, o_kv);
+      pl->qblocks = at<QBlock>(pl->bwd, o_qb);
+      pl->reduces = at<ReduceItem>(pl->bwd, o_red);
+      pl->n_kv = (int)kv.items.size();
+      pl->n_reduce = (int)kv.reduces.size();
+      pl->nslots = kv.nslots;
+    }
   }
-  if (need_bwd && !pl->bwd_ready) {
-    auto dq = plan_qtiles(L, dq_query_tile(D), dq_key_tile(D));
-    if (upload(&pl->dq_items, dq) != cudaSuccess) return DUALKV_ERR_CUDA;
-    pl->n_dq = (int)dq.size();
-    KVPlan kv = plan_kvtiles(L, dkv_key_tile(D), dkv_query_block(D), kMaxDkvIters);
-    if (upload(&pl->kv_items, kv.items) != cudaSuccess) return DUALKV_ERR_CUDA;
-    if (upload(&pl->qblocks, kv.qblocks) != cudaSuccess) return DUALKV_ERR_CUDA;
-    if (upload(&pl->reduces, kv.reduces) != cudaSuccess) return DUALKV_ERR_CUDA;
-    pl->n_kv = (int)kv.items.size();
-    pl->n_reduce = (int)kv.reduces.size();
-    pl->nslots = kv.nslots;
-    pl->bwd_ready = true;
-  }
+  if ((rc = wait_part(pl->fwd, st))) return rc;
+  if (need_bwd && (rc = wait_part(pl->bwd, st))) return rc;
   *out = pl;
   return DUALKV_OK;
 }
@@ -244,19 +407,31 @@ int make_block_tmap(CUtensorMap* m, const void* base, int64_t n_blocks, int box_
   return r == CUDA_SUCCESS ? DUALKV_OK : DUALKV_ERR_CUDA;
 }
 
-// Device copy of R_offsets and the SM count for the pack kernels; caller holds g_mu.
-int get_offsets(int P, int N, const int32_t* off, DevOffsets** out) {
+// Device copy of R_offsets and the SM count for the pack kernels, ordered on `st`
+// after its upload; caller holds g_mu.
+int get_offsets(int P, int N, const int32_t* off, cudaStream_t st, DevOffsets** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return DUALKV_ERR_CUDA;
-  auto& slot = g_offsets[plan_key(dev, P, N, off, 0, 0, 0, 0)];
-  if (!slot) {
-    std::unique_ptr<DevOffsets> o(new DevOffsets());
-    if (cudaDeviceGetAttribute(&o->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+  const std::string key = plan_key(dev, P, N, off, 0, 0, 0, 0);
+  DevOffsets* o = g_offsets.find(key);
+  if (!o) {
+    std::unique_ptr<DevOffsets> fresh(new DevOffsets());
+    if (cudaDeviceGetAttribute(&fresh->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return DUALKV_ERR_CUDA;
-    if (upload(&o->d, std::vector<int32_t>(off, off + N + 1)) != cudaSuccess) return DUALKV_ERR_CUDA;
-    slot = std::move(o);
+    Packer pk;
+    const size_t o_off = pk.add(std::vector<int32_t>(off, off + N + 1));
+    const int rc = upload_part(dev, pk, st, &fresh->part);
+    if (rc) {
+      retire_offsets(*fresh);
+      return rc;
+    }
+    fresh->d = at<int32_t>(fresh->part, o_off);
+    o = fresh.get();
+    insert_retiring(g_offsets, key, std::move(fresh), retire_offsets);
   }
-  *out = slot.get();
+  const int rc = wait_part(o->part, st);
+  if (rc) return rc;
+  *out = o;
   return DUALKV_OK;
 }
 
@@ -279,13 +454,13 @@ int pack_call(int kind, const void* src, void* dst, int P, int N, const int32_t*
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   std::lock_guard<std::mutex> lock(g_mu);
   DevOffsets* o = nullptr;
-  int rc = get_offsets(P, N, off, &o);
+  int rc = get_offsets(P, N, off, st, &o);
   if (rc) return rc;
   if (timed(DUALKV_KERNEL_PACK, st, [&] {
         return launch_pack(kind, src, dst, o->d, P, N, T, row_elems, o->num_sms, st);
       }) != cudaSuccess)
     return DUALKV_ERR_CUDA;
-  return DUALKV_OK;
+  return mark_use(&o->last_use, st);
 }
 
 bool supported_d(int D) { return D == 64 || D == 128 || D == 512; }  // backward
@@ -300,11 +475,12 @@ int fwd_impl(const void* q, const void* k, const void* v, int P, int N, const in
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse)) return DUALKV_ERR_ALIGN;
   if (!supported_fwd_d(D)) return DUALKV_ERR_UNSUPPORTED;
   const int64_t T = (int64_t)P + R_offsets[N];
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
   std::lock_guard<std::mutex> lock(g_mu);
   int rc = ensure_encode();
   if (rc) return rc;
   DevPlan* pl = nullptr;
-  if ((rc = get_plan(P, N, R_offsets, Hq, Hkv, D, window, kv_lo, kv_hi, false, &pl))) return rc;
+  if ((rc = get_plan(P, N, R_offsets, Hq, Hkv, D, window, kv_lo, kv_hi, false, st, &pl))) return rc;
   uint32_t* status = nullptr;
   if ((rc = status_word(pl->device, &status))) return rc;
   CUtensorMap tq, tk, tv;
@@ -313,10 +489,9 @@ int fwd_impl(const void* q, const void* k, const void* v, int P, int N, const in
     return DUALKV_ERR_CUDA;
   FwdArgs a{pl->fwd_items, static_cast<__nv_bfloat16*>(out), lse, (int)T, Hq, Hkv, window <= 0 ? 0 : window,
             scale * 1.4426950408889634f, status};
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (timed(DUALKV_KERNEL_FWD, st, [&] { return launch_fwd(D, tq, tk, tv, a, pl->n_fwd, st); }) != cudaSuccess)
     return DUALKV_ERR_CUDA;
-  return DUALKV_OK;
+  return mark_use(&pl->last_use, st);
 }
 
 int bwd_impl(const void* q, const void* k, const void* v, const void* out, const float* lse, const void* dout, int P,
@@ -337,7 +512,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
   int rc = ensure_encode();
   if (rc) return rc;
   DevPlan* pl = nullptr;
-  if ((rc = get_plan(P, N, R_offsets, Hq, Hkv, D, window, kv_lo, kv_hi, true, &pl))) return rc;
+  if ((rc = get_plan(P, N, R_offsets, Hq, Hkv, D, window, kv_lo, kv_hi, true, st, &pl))) return rc;
   const WsLayout ws = ws_layout(T, Hq, D, pl->nslots, D == 512 ? pl->n_blocks : 0);
   if (workspace_bytes < ws.total) return DUALKV_ERR_WORKSPACE;
   uint32_t* status = nullptr;
@@ -364,11 +539,14 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
         make_block_tmap(&tP64, pblk, pl->n_blocks, 64) || make_block_tmap(&tDS64, dsblk, pl->n_blocks, 64) ||
         make_block_tmap(&tDS128, dsblk, pl->n_blocks, 128))
       return DUALKV_ERR_CUDA;
-    PdsArgs p0{pl->dq_items, pl->block_base, lse2, delta, nullptr, pblk, (int)T, Hq, Hkv, W, sl2, status};
-    PdsArgs p1{pl->dq_items, pl->block_base, lse2, delta, pblk, dsblk, (int)T, Hq, Hkv, W, sl2, status};
-    XtgArgs xv{pl->xt_items, pl->xt_entries, static_cast<__nv_bfloat16*>(dv), partial, 1, (int)T, Hq, Hkv, 1.f, status};
-    XtgArgs xk{pl->xt_items, pl->xt_entries, static_cast<__nv_bfloat16*>(dk), partial, 0, (int)T, Hq, Hkv, scale, status};
-    Dq512Args qa{pl->dq_items, pl->block_base, static_cast<__nv_bfloat16*>(dq), (int)T, Hq, Hkv, scale, status};
+    PdsArgs p0{pl->dq_items, pl->block_base, lse2, delta, nullptr, pblk, (int)T, Hq, Hkv, W, sl2, status, pl->n_blocks};
+    PdsArgs p1{pl->dq_items, pl->block_base, lse2, delta, pblk, dsblk, (int)T, Hq, Hkv, W, sl2, status, pl->n_blocks};
+    XtgArgs xv{pl->xt_items, pl->xt_entries, static_cast<__nv_bfloat16*>(dv), partial, 1, (int)T, Hq, Hkv, 1.f, status,
+               pl->n_xt_entries, pl->n_blocks, pl->nslots};
+    XtgArgs xk{pl->xt_items, pl->xt_entries, static_cast<__nv_bfloat16*>(dk), partial, 0, (int)T, Hq, Hkv, scale, status,
+               pl->n_xt_entries, pl->n_blocks, pl->nslots};
+    Dq512Args qa{pl->dq_items, pl->block_base, static_cast<__nv_bfloat16*>(dq), (int)T, Hq, Hkv, scale, status,
+                 pl->n_blocks};
     if (timed(DUALKV_KERNEL_DKV, st, [&] {
           cudaError_t e = launch_pds(0, tq, tk, p0, pl->n_dq, st);
           if (e == cudaSuccess) e = launch_pds(1, tdo, tv, p1, pl->n_dq, st);
@@ -378,13 +556,14 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
         }) != cudaSuccess)
       return DUALKV_ERR_CUDA;
     if (pl->n_reduce > 0) {
-      ReduceArgs ra{pl->reduces, partial, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), Hkv, D, 128};
+      ReduceArgs ra{pl->reduces, partial, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), Hkv, D, 128,
+                    T, pl->nslots, status};
       if (timed(DUALKV_KERNEL_REDUCE, st, [&] { return launch_reduce(ra, pl->n_reduce, st); }) != cudaSuccess)
         return DUALKV_ERR_CUDA;
     }
     if (timed(DUALKV_KERNEL_DQ, st, [&] { return launch_dq512(tDS128, tk64, qa, pl->n_dq, st); }) != cudaSuccess)
       return DUALKV_ERR_CUDA;
-    return DUALKV_OK;
+    return mark_use(&pl->last_use, st);
   }
 
   CUtensorMap tq, tk, tv, tdo;
@@ -392,12 +571,12 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
       make_tmap(&tv, v, T, Hkv, D, dkv_key_tile(D)) || make_tmap(&tdo, dout, T, Hq, D, dkv_query_block(D)))
     return DUALKV_ERR_CUDA;
   DkvArgs ka{pl->kv_items, pl->qblocks, delta, lse2, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
-             partial, (int)T, Hq, Hkv, W, sl2, scale, status};
+             partial, (int)T, Hq, Hkv, W, sl2, scale, status, pl->nslots};
   if (timed(DUALKV_KERNEL_DKV, st, [&] { return launch_dkv(D, tq, tk, tv, tdo, ka, pl->n_kv, st); }) != cudaSuccess)
     return DUALKV_ERR_CUDA;
   if (pl->n_reduce > 0) {
     ReduceArgs ra{pl->reduces, partial, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), Hkv, D,
-                  dkv_key_tile(D)};
+                  dkv_key_tile(D), T, pl->nslots, status};
     if (timed(DUALKV_KERNEL_REDUCE, st, [&] { return launch_reduce(ra, pl->n_reduce, st); }) != cudaSuccess)
       return DUALKV_ERR_CUDA;
   }
@@ -409,7 +588,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
   DqArgs qa{pl->dq_items, delta, lse2, static_cast<__nv_bfloat16*>(dq), (int)T, Hq, Hkv, W, sl2, scale, status};
   if (timed(DUALKV_KERNEL_DQ, st, [&] { return launch_dq(D, tq2, tk2, tv2, tdo2, qa, pl->n_dq, st); }) != cudaSuccess)
     return DUALKV_ERR_CUDA;
-  return DUALKV_OK;
+  return mark_use(&pl->last_use, st);
 }
 
 }  // namespace
@@ -615,6 +794,89 @@ int dualkv_selftest_timeout(uint64_t limit_ns, void* stream) {
   return DUALKV_OK;
 }
 
+int dualkv_plan_cache_info(int* n_plans, int64_t* device_bytes) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (n_plans) *n_plans = (int)g_plans.size();
+  if (device_bytes) *device_bytes = (int64_t)g_blob_bytes;
+  return DUALKV_OK;
+}
+
+int dualkv_selftest_kernel(int which, uint64_t limit_ns, void* stream) {
+  if (which < 0 || which > 2) return DUALKV_ERR_INVALID;
+  if (limit_ns < 1000000ull || limit_ns > 10000000000ull) return DUALKV_ERR_INVALID;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_mu);
+  int rc = ensure_encode();
+  if (rc) return rc;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DUALKV_ERR_CUDA;
+  uint32_t* status = nullptr;
+  if ((rc = status_word(dev, &status))) return rc;
+  // a tiny layout with zero inputs: P = 128 and two responses of 128, one head, D = 128
+  constexpr int P = 128, N = 2, Hq = 1, Hkv = 1, D = 128;
+  const int32_t off[N + 1] = {0, 128, 256};
+  constexpr int64_t T = P + 256;
+  const float scale = 0.08838834764831845f;
+  DevPlan* pl = nullptr;
+  if ((rc = get_plan(P, N, off, Hq, Hkv, D, 0, 0, Hkv, which == 1, st, &pl))) return rc;
+  const size_t tensor_bytes = (size_t)T * Hq * D * 2;
+  const WsLayout ws = ws_layout(T, Hq, D, pl->nslots, 0);
+  uint8_t* mem = nullptr;
+  const size_t o_lse = 7 * tensor_bytes, o_ws = align256(o_lse + sizeof(float) * Hq * T),
+               o_items = o_ws + align256(ws.total), total = o_items + align256(sizeof(QTileItem) * pl->n_fwd);
+  if (cudaMalloc(&mem, total) != cudaSuccess) return DUALKV_ERR_CUDA;
+  auto done = [&](int code) {
+    cudaStreamSynchronize(st);
+    cudaFree(mem);
+    return code;
+  };
+  if (cudaMemsetAsync(mem, 0, total, st) != cudaSuccess) return done(DUALKV_ERR_CUDA);
+  void *q = mem, *k = mem + tensor_bytes, *v = mem + 2 * tensor_bytes, *out = mem + 3 * tensor_bytes,
+       *dout = mem + 4 * tensor_bytes, *dk = mem + 5 * tensor_bytes, *dv = mem + 6 * tensor_bytes;
+  float* lse = reinterpret_cast<float*>(mem + o_lse);
+  uint8_t* wsb = mem + o_ws;
+  CUtensorMap tq, tk, tv, tdo;
+  if (which != 1) {
+    // forward: every CTA waits for K/V unit 0, which is never loaded (which = 0), or the
+    // first work item is moved past the last row (which = 2)
+    const QTileItem* items = pl->fwd_items;
+    if (which == 2) {
+      Layout L{P, N, std::vector<int32_t>(off, off + N + 1), Hq, Hkv, D, 0};
+      std::vector<QTileItem> bad = plan_qtiles(L, fwd_query_tile(D), fwd_key_tile(D));
+      bad[0].q_row0 = (int32_t)T + 64;
+      QTileItem* d_items = reinterpret_cast<QTileItem*>(mem + o_items);
+      if (cudaMemcpyAsync(d_items, bad.data(), sizeof(QTileItem) * bad.size(), cudaMemcpyHostToDevice, st) !=
+              cudaSuccess ||
+          cudaStreamSynchronize(st) != cudaSuccess)
+        return done(DUALKV_ERR_CUDA);
+      items = d_items;
+    }
+    if (make_tmap(&tq, q, T, Hq, D, fwd_query_tile(D)) || make_tmap(&tk, k, T, Hkv, D, fwd_key_tile(D)) ||
+        make_tmap(&tv, v, T, Hkv, D, fwd_key_tile(D)))
+      return done(DUALKV_ERR_CUDA);
+    FwdArgs a{items, static_cast<__nv_bfloat16*>(out), lse, (int)T, Hq, Hkv, 0, scale * 1.4426950408889634f, status};
+    a.wait_limit_ns = limit_ns;
+    if (which == 0) a.test_skip_unit = 0;
+    if (launch_fwd(D, tq, tk, tv, a, pl->n_fwd, st) != cudaSuccess) return done(DUALKV_ERR_CUDA);
+    return done(mark_use(&pl->last_use, st));
+  }
+  // dK/dV: the first work item's first Q/dO block gets one arrival too few
+  float* delta = reinterpret_cast<float*>(wsb + ws.delta);
+  float* lse2 = reinterpret_cast<float*>(wsb + ws.lse2);
+  PrepArgs pa{static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, delta, lse2, T, Hq, D};
+  if (launch_prep(pa, st) != cudaSuccess) return done(DUALKV_ERR_CUDA);
+  if (make_tmap(&tq, q, T, Hq, D, dkv_query_block(D)) || make_tmap(&tk, k, T, Hkv, D, dkv_key_tile(D)) ||
+      make_tmap(&tv, v, T, Hkv, D, dkv_key_tile(D)) || make_tmap(&tdo, dout, T, Hq, D, dkv_query_block(D)))
+    return done(DUALKV_ERR_CUDA);
+  DkvArgs ka{pl->kv_items, pl->qblocks, delta, lse2, static_cast<__nv_bfloat16*>(dk),
+             static_cast<__nv_bfloat16*>(dv), reinterpret_cast<float*>(wsb + ws.partial), (int)T, Hq, Hkv, 0,
+             scale * 1.4426950408889634f, scale, status, pl->nslots};
+  ka.wait_limit_ns = limit_ns;
+  ka.test_skip_iter = 0;
+  if (launch_dkv(D, tq, tk, tv, tdo, ka, pl->n_kv, st) != cudaSuccess) return done(DUALKV_ERR_CUDA);
+  return done(mark_use(&pl->last_use, st));
+}
+
 int dualkv_profile_enable(int on) {
   std::lock_guard<std::mutex> lock(g_mu);
   g_profile = on != 0;
@@ -648,8 +910,16 @@ void dualkv_release(void) {
   g_timed.clear();
   for (cudaEvent_t e : g_event_pool) cudaEventDestroy(e);
   g_event_pool.clear();
-  g_plans.clear();
-  g_offsets.clear();
+  {
+    std::vector<std::unique_ptr<DevPlan>> plans;
+    g_plans.clear(&plans);
+    for (auto& p : plans) retire_plan(*p);
+    std::vector<std::unique_ptr<DevOffsets>> offs;
+    g_offsets.clear(&offs);
+    for (auto& o : offs) retire_offsets(*o);
+    for (Blob& b : g_free_blobs) free_blob(b);
+    g_free_blobs.clear();
+  }
   for (auto& kv : g_status) cudaFree(kv.second);
   g_status.clear();
 }

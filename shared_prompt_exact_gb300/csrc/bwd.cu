@@ -18,6 +18,7 @@
 // query tile; same key walk as the forward).
 #include <cuda_bf16.h>
 
+#include "checks.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -168,7 +169,10 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
 
   const uint32_t warp = warp_id(), lane = lane_id();
   FailState fs{&ctl.abort_flag, a.status};
-  auto tiles_of = [](const QTileItem& q) {
+  // key tiles of an item, or -1 for an item outside the tensors: every role skips it
+  // (nothing is read or written for it) and one thread records the violation
+  auto tiles_of = [&](const QTileItem& q) {
+    if (!qtile_ok(q, a.T, a.Hq, C::BM, C::BN)) return -1;
     return (q.reg[0].t_hi - q.reg[0].t_lo) + (q.reg[1].t_hi - q.reg[1].t_lo);
   };
 
@@ -216,7 +220,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
         const QTileItem it = a.items[item];
         const int nt = tiles_of(it);
-        if (nt == 0) continue;
+        if (nt <= 0) continue;
         const int kvh = it.head / (a.Hq / a.Hkv);
         // Q / dO are overwritten only after every GEMM of the previous item has completed
         if (kx > 0 && !(ok = mbar_wait(&ctl.q_free, (kx - 1) & 1, fs))) break;
@@ -269,7 +273,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     int g = 0, kx = 0;
     for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
       const int nt = tiles_of(a.items[item]);
-      if (nt == 0) continue;
+      if (nt <= 0) continue;
       // Q copied into TMEM (after its TMA load, which also brought dO)
       if (!(ok = mbar_wait(&ctl.q_tmem, kx & 1, fs))) break;
       ++kx;
@@ -320,7 +324,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     int g = 0, kx = 0;
     for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
       const int nt = tiles_of(a.items[item]);
-      if (nt == 0) continue;
+      if (nt <= 0) continue;
       for (int j = 0; j < nt && ok; ++j, ++g) {
         const int ks = g % C::NSK;
         if (!(ok = mbar_wait(&ctl.ds_full, g & 1, fs))) break;
@@ -356,6 +360,10 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
       const QTileItem it = a.items[item];
       const int nt = tiles_of(it);
+      if (nt < 0) {
+        if (warp == 2 && lane == 0 && a.status) atomicOr(a.status, kDevErrBounds);
+        continue;
+      }
       const int qpos = it.q_pos0 + row;
       const bool valid = row < it.q_rows;
       // this warp writes dQ columns [grp * D / NG, (grp + 1) * D / NG) of its row
@@ -531,12 +539,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* sRing = smem + C::OFF_RING;
 
   const KVTileItem it = a.items[blockIdx.x];
-  const int n_iter = it.it_hi - it.it_lo;
   const int gs = a.Hq / a.Hkv;
+  // an item outside the tensors (key rows, kv-head, its span of the query list or its
+  // partial slot) is recorded and does nothing; a query block outside them is caught
+  // by the producer before its loads
+  const bool item_ok = rows_ok(it.k_row0, it.k_rows, a.T, C::BN) && it.kv_head >= 0 && it.kv_head < a.Hkv &&
+                       it.list_begin >= 0 && it.it_lo >= 0 && it.it_lo <= it.it_hi &&
+                       it.it_hi <= gs * it.list_len && it.partial_slot >= -1 && it.partial_slot < a.nslots;
+  const int n_iter = item_ok ? it.it_hi - it.it_lo : 0;
   const uint32_t warp = warp_id(), lane = lane_id();
-  FailState fs{&ctl.abort_flag, a.status};
+  FailState fs{&ctl.abort_flag, a.status, a.wait_limit_ns};
+  // failure-path self-test: iteration whose Q/dO block gets one arrival too few
+  const int skip_iter = blockIdx.x == 0 ? a.test_skip_iter : -1;
 
   if (threadIdx.x == 0) {
+    if (!item_ok && a.status) atomicOr(a.status, kDevErrBounds);
     ctl.abort_flag = 0;
     mbar_init(&ctl.kv_full, 1);
     for (int i = 0; i < C::NST; ++i) {
@@ -584,10 +601,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int itx = it.it_lo + idx;
         h = it.kv_head * gs + itx % gs;
         qb = a.qblocks[it.list_begin + itx / gs];
+        const bool qb_ok = rows_ok(qb.q_row0, qb.q_rows, a.T, C::BQ);
+        if (!qb_ok) qb.q_rows = -1;  // marks the block as outside the tensors
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int c = (int)lane + 32 * e;
-          const bool v = c < qb.q_rows;
+          const bool v = qb_ok && c < qb.q_rows;
           const int64_t rix = (int64_t)h * a.T + qb.q_row0 + c;
           l2[e] = v ? a.lse2[rix] : INFINITY;
           dl[e] = v ? a.delta[rix] : 0.f;
@@ -599,8 +618,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       fetch(0, h, qb, l2, dl);
       for (; i < n_iter; ++i) {
         const int slot = i % C::NST;
+        if (qb.q_rows < 0) {
+          raise_failure(fs, kDevErrBounds);
+          ok = false;
+          break;
+        }
         if (!(ok = mbar_wait(&ctl.ring_empty[slot], ((i / C::NST) & 1) ^ 1, fs))) break;
-        if (lane == 0) {
+        if (lane == 0 && i != skip_iter) {
           mbar_arrive_expect_tx(&ctl.ring_full[slot], C::UNIT_BYTES);
           uint8_t* dst = sRing + slot * C::UNIT_BYTES;
           for (int c = 0; c < C::KCH; ++c) {
@@ -622,6 +646,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_wait_drain(&ctl.kv_full, 0, kWaitLimitNs);
         for (int back = 1; back <= C::NST && back <= i; ++back) {
           const int i2 = i - back;
+          if (i2 == skip_iter) continue;  // never completes: nothing was loaded for it
           mbar_wait_drain(&ctl.ring_full[i2 % C::NST], (i2 / C::NST) & 1, kWaitLimitNs);
         }
       }
@@ -799,7 +824,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.ds_full[b]);
     }
-    if (ok) {
+    if (ok && item_ok) {
       if (n_iter > 0) {
         ok = mbar_wait(&ctl.acc_done, 0, fs);
         tc_fence_after();
@@ -857,6 +882,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 constexpr int kReduceThreads = 256;
 __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(const ReduceArgs a) {
   const ReduceItem it = a.items[blockIdx.x];
+  if (!(rows_ok(it.k_row0, it.k_rows, a.T, a.key_tile) && it.kv_head >= 0 && it.kv_head < a.Hkv && it.slot0 >= 0 &&
+        it.nslots >= 0 && it.slot0 + it.nslots <= a.total_slots)) {
+    if (threadIdx.x == 0 && blockIdx.y == 0 && a.status) atomicOr(a.status, kDevErrBounds);
+    return;
+  }
   const int v4_per_row = a.D / 4;
   const int e4 = blockIdx.y * kReduceThreads + threadIdx.x;  // float4 index inside the tile
   const int j = e4 / v4_per_row, d = (e4 % v4_per_row) * 4;
@@ -887,8 +917,8 @@ __global__ void __launch_bounds__(64) selftest_timeout_kernel(uint64_t limit_ns,
   }
   __syncthreads();
   if (threadIdx.x == 0) mbar_arrive(&never);
-  FailState fs{&abort_flag, status};
-  mbar_wait(&never, 0, fs, limit_ns);
+  FailState fs{&abort_flag, status, limit_ns};
+  mbar_wait(&never, 0, fs);
   __syncthreads();
 }
 

@@ -14,6 +14,7 @@
 // segment) that attend a prompt key tile, in the fixed order of the plan.
 #include <cuda_bf16.h>
 
+#include "checks.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -78,12 +79,16 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
 
   const QTileItem it = a.items[blockIdx.x];
   const int blk0 = a.block_base[blockIdx.x];
-  const int nt = (it.reg[0].t_hi - it.reg[0].t_lo) + (it.reg[1].t_hi - it.reg[1].t_lo);
+  const int nt_all = (it.reg[0].t_hi - it.reg[0].t_lo) + (it.reg[1].t_hi - it.reg[1].t_lo);
+  // an item outside the tensors or naming blocks past the block array does nothing
+  const bool item_ok = qtile_ok(it, a.T, a.Hq, C::BM, C::BN) && blk0 >= 0 && (int64_t)blk0 + nt_all <= a.n_blocks;
+  const int nt = item_ok ? nt_all : 0;
   const int kvh = it.head / (a.Hq / a.Hkv);
   const uint32_t warp = warp_id(), lane = lane_id();
   FailState fs{&ctl.abort_flag, a.status};
 
   if (threadIdx.x == 0) {
+    if (!item_ok && a.status) atomicOr(a.status, kDevErrBounds);
     ctl.abort_flag = 0;
     mbar_init(&ctl.a_full, 1);
     mbar_init(&ctl.a_tmem, 8);
@@ -304,11 +309,18 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ XtgCtl ctl;
   const XTItem it = a.items[blockIdx.x];
-  const int n_iter = it.it_hi - it.it_lo;
+  // an item outside the tensors does nothing; an entry outside them is caught by the
+  // producer before its loads
+  const bool item_ok = rows_ok(it.k_row0, it.k_rows, a.T, 128) && it.kv_head >= 0 && it.kv_head < a.Hkv &&
+                       it.list_begin >= 0 && it.it_lo >= 0 && it.it_lo <= it.it_hi &&
+                       (int64_t)it.list_begin + it.it_hi <= a.n_entries && it.partial_slot >= -1 &&
+                       it.partial_slot < a.nslots;
+  const int n_iter = item_ok ? it.it_hi - it.it_lo : 0;
   const uint32_t warp = warp_id(), lane = lane_id();
   FailState fs{&ctl.abort_flag, a.status};
 
   if (threadIdx.x == 0) {
+    if (!item_ok && a.status) atomicOr(a.status, kDevErrBounds);
     ctl.abort_flag = 0;
     for (int i = 0; i < C::NST; ++i) {
       mbar_init(&ctl.full[i], 1);
@@ -334,6 +346,13 @@ __global__ void __launch_bounds__(192, 1)
       for (; i < n_iter; ++i) {
         const XTEntry e = a.entries[it.list_begin + it.it_lo + i];
         const int slot = i % C::NST;
+        const int gs = a.Hq / a.Hkv;
+        if (!(e.head >= it.kv_head * gs && e.head < (it.kv_head + 1) * gs && rows_ok(e.q_row0, 1, a.T, 1) &&
+              e.block >= 0 && e.block < a.n_blocks && (e.sub == 0 || e.sub == 1))) {
+          raise_failure(fs, kDevErrBounds);
+          ok = false;
+          break;
+        }
         if (!(ok = mbar_wait(&ctl.empty[slot], ((i / C::NST) & 1) ^ 1, fs))) break;
         mbar_arrive_expect_tx(&ctl.full[slot], C::STAGE_BYTES);
         uint8_t* st = smem + slot * C::STAGE_BYTES;
@@ -385,8 +404,8 @@ __global__ void __launch_bounds__(192, 1)
     const int row = (int)(wq * 32 + lane);
     const uint32_t tl = tmem + ((wq * 32) << 16);
     const bool kvalid = row < it.k_rows;
-    bool ok = true;
-    if (n_iter > 0) {
+    bool ok = item_ok;
+    if (ok && n_iter > 0) {
       ok = mbar_wait(&ctl.acc_done, 0, fs);
       tc_fence_after();
     }
@@ -451,13 +470,17 @@ __global__ void __launch_bounds__(192, 1)
   __shared__ XtgCtl ctl;
   const QTileItem it = a.items[blockIdx.x];
   const int blk0 = a.block_base[blockIdx.x];
-  const int nt = (it.reg[0].t_hi - it.reg[0].t_lo) + (it.reg[1].t_hi - it.reg[1].t_lo);
+  const int nt_all = (it.reg[0].t_hi - it.reg[0].t_lo) + (it.reg[1].t_hi - it.reg[1].t_lo);
+  // an item outside the tensors or naming blocks past the block array does nothing
+  const bool item_ok = qtile_ok(it, a.T, a.Hq, 128, 128) && blk0 >= 0 && (int64_t)blk0 + nt_all <= a.n_blocks;
+  const int nt = item_ok ? nt_all : 0;
   const int n_iter = 2 * nt;
   const int kvh = it.head / (a.Hq / a.Hkv);
   const uint32_t warp = warp_id(), lane = lane_id();
   FailState fs{&ctl.abort_flag, a.status};
 
   if (threadIdx.x == 0) {
+    if (!item_ok && a.status) atomicOr(a.status, kDevErrBounds);
     ctl.abort_flag = 0;
     for (int i = 0; i < C::NST; ++i) {
       mbar_init(&ctl.full[i], 1);

@@ -38,6 +38,7 @@
 // both compute the full S = Q K^T (contraction over all 512 columns).
 #include <cuda_bf16.h>
 
+#include "checks.cuh"
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -109,13 +110,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 
   const QTileItem it = a.items[blockIdx.x / C::NSPLIT];
   const int split = (int)(blockIdx.x % C::NSPLIT);
+  // an item outside the tensors is recorded and given no key tiles: nothing is read or written
+  const bool item_ok = qtile_ok(it, a.T, a.Hq, C::BM, C::BN);
   const int nt0 = it.reg[0].t_hi - it.reg[0].t_lo;
-  const int nt = nt0 + (it.reg[1].t_hi - it.reg[1].t_lo);
+  const int nt = item_ok ? nt0 + (it.reg[1].t_hi - it.reg[1].t_lo) : 0;
   const int kvh = it.head / (a.Hq / a.Hkv);
   const uint32_t warp = warp_id(), lane = lane_id();
-  FailState fs{&ctl.abort_flag, a.status};
+  FailState fs{&ctl.abort_flag, a.status, a.wait_limit_ns};
 
   if (threadIdx.x == 0) {
+    if (!item_ok && a.status) atomicOr(a.status, kDevErrBounds);
     ctl.abort_flag = 0;
     mbar_init(&ctl.q_full, 1);
     for (int i = 0; i < C::NST; ++i) {
@@ -168,6 +172,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
           for (int u = 0; u < nu; ++u, ++idx) {
             const int slot = idx % C::NST;
             if (!(ok = mbar_wait(&ctl.ring_empty[slot], ((idx / C::NST) & 1) ^ 1, fs))) break;
+            if (idx == a.test_skip_unit) continue;  // failure-path self-test: never loaded
             mbar_arrive_expect_tx(&ctl.ring_full[slot], C::UNIT_BYTES);
             uint8_t* dst = sRing + slot * C::UNIT_BYTES;
             for (int c = 0; c < C::UCH; ++c)
@@ -180,6 +185,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
         mbar_wait_drain(&ctl.q_full, 0, kWaitLimitNs);
         for (int back = 1; back <= C::NST && back <= idx; ++back) {
           const int i2 = idx - back;
+          if (i2 == a.test_skip_unit) continue;
           mbar_wait_drain(&ctl.ring_full[i2 % C::NST], (i2 / C::NST) & 1, kWaitLimitNs);
         }
       }

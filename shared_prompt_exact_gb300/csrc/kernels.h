@@ -9,6 +9,9 @@
 
 namespace dkv {
 
+// Limit of every bounded wait in a normal launch (a healthy wait ends in microseconds).
+constexpr uint64_t kLaunchWaitLimitNs = 2000000000ull;
+
 struct FwdArgs {
   const QTileItem* items;
   __nv_bfloat16* out;
@@ -16,6 +19,10 @@ struct FwdArgs {
   int T, Hq, Hkv, window;
   float scale_log2;  // softmax scale * log2(e)
   uint32_t* status;
+  uint64_t wait_limit_ns = kLaunchWaitLimitNs;
+  // failure-path self-test only (-1 otherwise): the K/V ring unit with this index is
+  // never loaded, so the wait for it runs out after wait_limit_ns
+  int test_skip_unit = -1;
 };
 
 // Query tile rows / key tile size of the forward kernel for head dimension D.
@@ -64,6 +71,11 @@ struct DkvArgs {
   float scale_log2;
   float scale;
   uint32_t* status;
+  int nslots = 0;  // partial slots in `partial` (work items naming another slot are out of range)
+  uint64_t wait_limit_ns = kLaunchWaitLimitNs;
+  // failure-path self-test only (-1 otherwise): the Q/dO block of this iteration of
+  // the first work item gets one arrival too few, so the wait for it runs out
+  int test_skip_iter = -1;
 };
 int dkv_key_tile(int D);
 int dkv_query_block(int D);
@@ -76,6 +88,9 @@ struct ReduceArgs {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int Hkv, D, key_tile;
+  int64_t T = 0;        // rows of dk / dv
+  int total_slots = 0;  // partial slots in `partial`
+  uint32_t* status = nullptr;
 };
 cudaError_t launch_reduce(const ReduceArgs& a, int n_items, cudaStream_t st);
 
@@ -90,6 +105,7 @@ struct PdsArgs {
   int T, Hq, Hkv, window;
   float scale_log2;
   uint32_t* status;
+  int64_t n_blocks = 0;  // P / dS blocks in p_blocks and out_blocks
 };
 cudaError_t launch_pds(int mode, const CUtensorMap& tA, const CUtensorMap& tB, const PdsArgs& a, int n_items,
                        cudaStream_t st);
@@ -103,6 +119,9 @@ struct XtgArgs {
   int T, Hq, Hkv;
   float mul;
   uint32_t* status;
+  int64_t n_entries = 0;  // entries in `entries`
+  int64_t n_blocks = 0;   // P / dS blocks the entries may name
+  int nslots = 0;         // partial slots in `partial`
 };
 cudaError_t launch_xtg(const CUtensorMap& tBlk, const CUtensorMap& tB, const XtgArgs& a, int n_items, cudaStream_t st);
 
@@ -113,6 +132,7 @@ struct Dq512Args {
   int T, Hq, Hkv;
   float scale;
   uint32_t* status;
+  int64_t n_blocks = 0;  // dS blocks
 };
 cudaError_t launch_dq512(const CUtensorMap& tBlk, const CUtensorMap& tK, const Dq512Args& a, int n_items,
                          cudaStream_t st);

@@ -130,42 +130,49 @@ extern "C" int dualkv_bwd_noalloc(const void* q, const void* k, const void* v, c
   if (rc) return rc;
   uint32_t* status = reinterpret_cast<uint32_t*>(base);
 
+  // From the first queued operation on, every exit waits for the work already on
+  // `stream`: the next call may come from another stream once the lock is released,
+  // and must not overlap copies or kernels of this one that still use the scratch.
+  auto fail = [&](int code) {
+    cudaStreamSynchronize(st);
+    return code;
+  };
   // the status word must start at zero; every other region is fully written before it is read
-  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), st) != cudaSuccess) return DUALKV_ERR_CUDA;
+  if (cudaMemsetAsync(status, 0, sizeof(uint32_t), st) != cudaSuccess) return fail(DUALKV_ERR_CUDA);
   if (put(base + o_dq, dq_items, st) != cudaSuccess || put(base + o_kv, kv.items, st) != cudaSuccess ||
       put(base + o_qb, kv.qblocks, st) != cudaSuccess || put(base + o_red, kv.reduces, st) != cudaSuccess)
-    return DUALKV_ERR_CUDA;
+    return fail(DUALKV_ERR_CUDA);
   float* delta = reinterpret_cast<float*>(base + o_delta);
   float* lse2 = reinterpret_cast<float*>(base + o_lse2);
   float* partial = reinterpret_cast<float*>(base + o_part);
   const float sl2 = scale * 1.4426950408889634f;
 
   PrepArgs pa{static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, delta, lse2, T, Hq, D};
-  if (launch_prep(pa, st) != cudaSuccess) return DUALKV_ERR_CUDA;
+  if (launch_prep(pa, st) != cudaSuccess) return fail(DUALKV_ERR_CUDA);
   CUtensorMap tq, tk, tv, tdo;
   if (tmap(&tq, q, T, Hq, D, dkv_query_block(D)) || tmap(&tk, k, T, Hkv, D, dkv_key_tile(D)) ||
       tmap(&tv, v, T, Hkv, D, dkv_key_tile(D)) || tmap(&tdo, dout, T, Hq, D, dkv_query_block(D)))
-    return DUALKV_ERR_CUDA;
+    return fail(DUALKV_ERR_CUDA);
   DkvArgs ka{reinterpret_cast<const KVTileItem*>(base + o_kv), reinterpret_cast<const QBlock*>(base + o_qb), delta,
              lse2, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), partial, (int)T, Hq, Hkv, W, sl2,
-             scale, status};
-  if (launch_dkv(D, tq, tk, tv, tdo, ka, (int)kv.items.size(), st) != cudaSuccess) return DUALKV_ERR_CUDA;
+             scale, status, kv.nslots};
+  if (launch_dkv(D, tq, tk, tv, tdo, ka, (int)kv.items.size(), st) != cudaSuccess) return fail(DUALKV_ERR_CUDA);
   if (!kv.reduces.empty()) {
     ReduceArgs ra{reinterpret_cast<const ReduceItem*>(base + o_red), partial, static_cast<__nv_bfloat16*>(dk),
-                  static_cast<__nv_bfloat16*>(dv), Hkv, D, dkv_key_tile(D)};
-    if (launch_reduce(ra, (int)kv.reduces.size(), st) != cudaSuccess) return DUALKV_ERR_CUDA;
+                  static_cast<__nv_bfloat16*>(dv), Hkv, D, dkv_key_tile(D), T, kv.nslots, status};
+    if (launch_reduce(ra, (int)kv.reduces.size(), st) != cudaSuccess) return fail(DUALKV_ERR_CUDA);
   }
   CUtensorMap tq2, tk2, tv2, tdo2;
   if (tmap(&tq2, q, T, Hq, D, dq_query_tile(D)) || tmap(&tk2, k, T, Hkv, D, dq_key_tile(D)) ||
       tmap(&tv2, v, T, Hkv, D, dq_key_tile(D)) || tmap(&tdo2, dout, T, Hq, D, dq_query_tile(D)))
-    return DUALKV_ERR_CUDA;
+    return fail(DUALKV_ERR_CUDA);
   DqArgs qa{reinterpret_cast<const QTileItem*>(base + o_dq), delta, lse2, static_cast<__nv_bfloat16*>(dq), (int)T, Hq,
             Hkv, W, sl2, scale, status};
-  if (launch_dq(D, tq2, tk2, tv2, tdo2, qa, (int)dq_items.size(), st) != cudaSuccess) return DUALKV_ERR_CUDA;
+  if (launch_dq(D, tq2, tk2, tv2, tdo2, qa, (int)dq_items.size(), st) != cudaSuccess) return fail(DUALKV_ERR_CUDA);
 
   // device-side failures land in the scratch's status word: read it once the pass is done
   uint32_t h = 0;
-  if (cudaMemcpyAsync(&h, status, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess) return DUALKV_ERR_CUDA;
+  if (cudaMemcpyAsync(&h, status, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess) return fail(DUALKV_ERR_CUDA);
   if (cudaStreamSynchronize(st) != cudaSuccess) return DUALKV_ERR_CUDA;
   return h ? DUALKV_ERR_DEVICE : DUALKV_OK;
 }

@@ -62,11 +62,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Kernel-wide failure state: a CTA-local abort flag in shared memory and the
-// launch's status word in global memory.
+// Kernel-wide failure state: a CTA-local abort flag in shared memory, the
+// launch's status word in global memory and the limit of every wait.
 struct FailState {
   volatile int* abort_flag;  // shared memory
   uint32_t* status;          // global memory, may be null
+  uint64_t limit_ns = kWaitLimitNs;
 };
 
 __device__ __forceinline__ void raise_failure(const FailState& fs, uint32_t code) {
@@ -76,8 +77,8 @@ __device__ __forceinline__ void raise_failure(const FailState& fs, uint32_t code
 
 // Bounded wait for phase `parity` of `bar`.  Returns false on timeout or when
 // another role of the CTA already aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const FailState& fs,
-                                          uint64_t limit_ns = kWaitLimitNs) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const FailState& fs) {
+  const uint64_t limit_ns = fs.limit_ns;
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {

@@ -32,7 +32,8 @@ EXPORTS = ("dualkv_fwd", "dualkv_bwd_workspace_bytes", "dualkv_bwd", "dualkv_bui
            "dualkv_pairs", "dualkv_check_status", "dualkv_error_string", "dualkv_profile_enable",
            "dualkv_profile_read", "dualkv_selftest_timeout", "dualkv_bwd_noalloc", "dualkv_release",
            "dualkv_pack", "dualkv_unpack", "dualkv_fold", "dualkv_fwd_heads", "dualkv_bwd_heads",
-           "dualkv_fwd_layers", "dualkv_bwd_layers", "dualkv_bwd_layers_workspace_bytes")
+           "dualkv_fwd_layers", "dualkv_bwd_layers", "dualkv_bwd_layers_workspace_bytes",
+           "dualkv_selftest_kernel", "dualkv_plan_cache_info")
 NOALLOC_SCRATCH_BYTES = 32 << 20
 KERNEL_KINDS = ("fwd", "prep", "dkv", "reduce", "dq", "pack")
 
@@ -88,6 +89,10 @@ def load(path: Optional[str] = None):
         lib.dualkv_bwd_noalloc.restype = ci
         lib.dualkv_selftest_timeout.argtypes = [ctypes.c_uint64, vp]
         lib.dualkv_selftest_timeout.restype = ci
+        lib.dualkv_selftest_kernel.argtypes = [ci, ctypes.c_uint64, vp]
+        lib.dualkv_selftest_kernel.restype = ci
+        lib.dualkv_plan_cache_info.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int64)]
+        lib.dualkv_plan_cache_info.restype = ci
         for name in ("dualkv_pack", "dualkv_unpack", "dualkv_fold"):
             getattr(lib, name).argtypes = [vp, vp, ci, ci, i32p, ci, vp]
             getattr(lib, name).restype = ci
@@ -136,12 +141,32 @@ def _check_dev(name, t, dtype):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _check_shapes(where, P, N, R_offsets, Hq, Hkv, D, **tensors):
+    """Every attention tensor must have exactly its layout's shape: q, out, dout, dq
+    (T, Hq, D); k, v, dk, dv (T, Hkv, D); lse (Hq, T), with T = P + R_offsets[N].  The
+    library builds its TMA views from these sizes, so an undersized tensor would be read
+    or written past its end; the check runs before anything reaches the C ABI."""
+    N = int(N)
+    if N < 1 or len(R_offsets) != N + 1:
+        raise ValueError(f"{where}: R_offsets must hold N + 1 = {N + 1} entries, got {len(R_offsets)}")
+    T = int(P) + int(R_offsets[N])
+    want = {"q": (T, Hq, D), "out": (T, Hq, D), "dout": (T, Hq, D), "dq": (T, Hq, D),
+            "k": (T, Hkv, D), "v": (T, Hkv, D), "dk": (T, Hkv, D), "dv": (T, Hkv, D), "lse": (Hq, T)}
+    for name, t in tensors.items():
+        shape = tuple(int(x) for x in want[name.split("[")[0]])
+        if not isinstance(t, torch.Tensor):
+            raise ValueError(f"{where}: {name} must be a tensor")
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{where}: {name} must have shape {shape} for this layout, got {tuple(t.shape)}")
+
+
 def _raise(code, where):
     if code != DUALKV_OK:
         raise DualKVError(code, where)
 
 
 def dualkv_fwd(q, k, v, P, N, R_offsets, Hq, Hkv, D, scale, window, out, lse, stream=None) -> None:
+    _check_shapes("dualkv_fwd", P, N, R_offsets, Hq, Hkv, D, q=q, k=k, v=v, out=out, lse=lse)
     for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
                         ("out", out, torch.bfloat16), ("lse", lse, torch.float32)):
         _check_dev(name, t, dt)
@@ -158,6 +183,8 @@ def dualkv_bwd_workspace_bytes(P, N, R_offsets, Hq, Hkv, D, window) -> int:
 
 def dualkv_bwd(q, k, v, out, lse, dout, P, N, R_offsets, Hq, Hkv, D, scale, window, dq, dk, dv, workspace,
                workspace_bytes=None, stream=None) -> None:
+    _check_shapes("dualkv_bwd", P, N, R_offsets, Hq, Hkv, D, q=q, k=k, v=v, out=out, lse=lse, dout=dout, dq=dq,
+                  dk=dk, dv=dv)
     for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
                         ("out", out, torch.bfloat16), ("lse", lse, torch.float32), ("dout", dout, torch.bfloat16),
                         ("dq", dq, torch.bfloat16), ("dk", dk, torch.bfloat16), ("dv", dv, torch.bfloat16)):
@@ -173,6 +200,7 @@ def dualkv_bwd(q, k, v, out, lse, dout, P, N, R_offsets, Hq, Hkv, D, scale, wind
 def dualkv_fwd_heads(q, k, v, P, N, R_offsets, Hq, Hkv, D, scale, window, kv_head_begin, kv_head_end, out, lse,
                      stream=None) -> None:
     """dualkv_fwd restricted to kv-heads [kv_head_begin, kv_head_end) and their q-heads."""
+    _check_shapes("dualkv_fwd_heads", P, N, R_offsets, Hq, Hkv, D, q=q, k=k, v=v, out=out, lse=lse)
     for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
                         ("out", out, torch.bfloat16), ("lse", lse, torch.float32)):
         _check_dev(name, t, dt)
@@ -185,6 +213,8 @@ def dualkv_fwd_heads(q, k, v, P, N, R_offsets, Hq, Hkv, D, scale, window, kv_hea
 def dualkv_bwd_heads(q, k, v, out, lse, dout, P, N, R_offsets, Hq, Hkv, D, scale, window, kv_head_begin,
                      kv_head_end, dq, dk, dv, workspace, workspace_bytes=None, stream=None) -> None:
     """dualkv_bwd restricted to kv-heads [kv_head_begin, kv_head_end) and their q-heads."""
+    _check_shapes("dualkv_bwd_heads", P, N, R_offsets, Hq, Hkv, D, q=q, k=k, v=v, out=out, lse=lse, dout=dout,
+                  dq=dq, dk=dk, dv=dv)
     for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
                         ("out", out, torch.bfloat16), ("lse", lse, torch.float32), ("dout", dout, torch.bfloat16),
                         ("dq", dq, torch.bfloat16), ("dk", dk, torch.bfloat16), ("dv", dv, torch.bfloat16)):
@@ -196,6 +226,14 @@ def dualkv_bwd_heads(q, k, v, out, lse, dout, P, N, R_offsets, Hq, Hkv, D, scale
                                  int(kv_head_begin), int(kv_head_end), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
                                  int(workspace_bytes), _stream(stream))
     _raise(rc, "dualkv_bwd_heads")
+
+
+def _check_layer_shapes(where, n, P, N, R_offsets, Hq, Hkv, D, **stacks):
+    for name, ts in stacks.items():
+        if len(ts) != n:
+            raise ValueError(f"{where}: {name}: expected {n} tensors, got {len(ts)}")
+        for i, t in enumerate(ts):
+            _check_shapes(where, P, N, R_offsets, Hq, Hkv, D, **{f"{name}[{i}]": t})
 
 
 def _ptr_array(name, tensors, n, dtype):
@@ -215,6 +253,7 @@ def dualkv_bwd_layers_workspace_bytes(windows, P, N, R_offsets, Hq, Hkv, D) -> i
 def dualkv_fwd_layers(qs, ks, vs, windows, P, N, R_offsets, Hq, Hkv, D, scale, outs, lses, stream=None) -> None:
     """Forward of a layer stack: layer l uses qs[l], ks[l], vs[l] and windows[l]."""
     n = len(windows)
+    _check_layer_shapes("dualkv_fwd_layers", n, P, N, R_offsets, Hq, Hkv, D, q=qs, k=ks, v=vs, out=outs, lse=lses)
     bf = torch.bfloat16
     rc = load().dualkv_fwd_layers(n, _ptr_array("q", qs, n, bf), _ptr_array("k", ks, n, bf), _ptr_array("v", vs, n, bf),
                                   (ctypes.c_int32 * n)(*[int(x) for x in windows]), int(P), int(N),
@@ -228,6 +267,8 @@ def dualkv_bwd_layers(qs, ks, vs, outs, lses, douts, windows, P, N, R_offsets, H
                       workspace, workspace_bytes=None, stream=None) -> None:
     """Backward of a layer stack, layers in the order given, one shared workspace."""
     n = len(windows)
+    _check_layer_shapes("dualkv_bwd_layers", n, P, N, R_offsets, Hq, Hkv, D, q=qs, k=ks, v=vs, out=outs, lse=lses,
+                        dout=douts, dq=dqs, dk=dks, dv=dvs)
     bf = torch.bfloat16
     if workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size()
@@ -262,6 +303,8 @@ def dualkv_bwd_noalloc(q, k, v, out, lse, dout, P, N, R_offsets, Hq, Hkv, D, sca
     memory.  Its scratch is a fixed array inside the library (NOALLOC_SCRATCH_BYTES
     per GPU); calls overlapping on the GPU race on it.  Returns once the pass has
     finished on `stream`."""
+    _check_shapes("dualkv_bwd_noalloc", P, N, R_offsets, Hq, Hkv, D, q=q, k=k, v=v, out=out, lse=lse, dout=dout,
+                  dq=dq, dk=dk, dv=dv)
     for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
                         ("out", out, torch.bfloat16), ("lse", lse, torch.float32), ("dout", dout, torch.bfloat16),
                         ("dq", dq, torch.bfloat16), ("dk", dk, torch.bfloat16), ("dv", dv, torch.bfloat16)):
@@ -348,6 +391,22 @@ def dualkv_profile_read():
 
 def dualkv_selftest_timeout(limit_ns: int, stream=None) -> None:
     _raise(load().dualkv_selftest_timeout(int(limit_ns), _stream(stream)), "dualkv_selftest_timeout")
+
+
+def dualkv_selftest_kernel(which: int, limit_ns: int, stream=None) -> None:
+    """Runs a production kernel on a tiny internal layout with its failure path
+    forced (0: forward, a K/V tile never loaded; 1: dK/dV, a query block one
+    barrier arrival short; 2: forward, a work item past the last row) and every
+    wait limited to limit_ns.  dualkv_check_status() then raises DUALKV_ERR_DEVICE."""
+    _raise(load().dualkv_selftest_kernel(int(which), int(limit_ns), _stream(stream)), "dualkv_selftest_kernel")
+
+
+def dualkv_plan_cache_info():
+    """(resident plans, device bytes held by the plan cache, resident and pooled)."""
+    n = ctypes.c_int(0)
+    b = ctypes.c_int64(0)
+    _raise(load().dualkv_plan_cache_info(ctypes.byref(n), ctypes.byref(b)), "dualkv_plan_cache_info")
+    return int(n.value), int(b.value)
 
 
 def dualkv_release() -> None:

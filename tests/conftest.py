@@ -24,3 +24,24 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+# Raw max-abs error of O (before the bf16 half-ulp allowance) per compared case,
+# printed at the end of the run so the stated 1e-2 bound is measured, not only
+# the allowance-adjusted check.
+_O_ERRORS = []
+
+
+@pytest.fixture
+def o_error_log():
+    def log(case, raw):
+        _O_ERRORS.append((str(case), float(raw)))
+    return log
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    if not _O_ERRORS:
+        return
+    terminalreporter.write_sep("-", "raw max-abs O error vs the fp64 oracle (bound 1e-2 before bf16 rounding)")
+    for case, raw in _O_ERRORS:
+        terminalreporter.write_line(f"{case}: {raw:.3e}")

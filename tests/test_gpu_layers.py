@@ -1,13 +1,15 @@
 """GPU tests of the layer-stack entry points dualkv_fwd_layers / dualkv_bwd_layers.
 
 A stack of sliding-window and global layers over one packed micro-batch must
-give, layer by layer, bitwise what separate dualkv_fwd / dualkv_bwd calls give
-(those are compared with the oracle by the parity tests), and must launch
-nothing when any layer's arguments are bad.
+match the fp64 oracle layer by layer (each layer with its own window), give
+bitwise what separate dualkv_fwd / dualkv_bwd calls give, and launch nothing
+when any layer's arguments are bad.
 """
 import pytest
 import torch
 
+import oracle
+from parity_checks import check_full
 from shared_prompt_exact_gb300 import build as pbuild
 from shared_prompt_exact_gb300 import dualkv
 from shared_prompt_exact_gb300 import workloads as wl
@@ -25,11 +27,15 @@ def _bits(t):
     return t.view(torch.int16 if t.dtype == torch.bfloat16 else torch.int32)
 
 
-def _layers(w, windows):
+def _layers(w, windows, host=None):
+    """Device inputs (q, k, v, dO) of each layer; with a list `host`, also their CPU copies."""
     layers = []
     for i, W in enumerate(windows):
         wi = wl.custom(w.P, w.R, w.Hq, w.Hkv, w.D, W, seed=w.seed + 101 * i)
-        layers.append(tuple(x.cuda() for x in wl.draw_inputs(wi)))
+        xs = wl.draw_inputs(wi)
+        if host is not None:
+            host.append(xs)
+        layers.append(tuple(x.cuda() for x in xs))
     return layers
 
 
@@ -41,10 +47,11 @@ CASES = [
 
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
-def test_stack_equals_single_layer_calls(case):
+def test_stack_equals_single_layer_calls(case, o_error_log):
     name, P, R, Hq, Hkv, D, windows = case
     w = wl.custom(P, R, Hq, Hkv, D, 0, seed=77)
-    layers = _layers(w, windows)
+    host = []
+    layers = _layers(w, windows, host)
     n = len(windows)
     qs, ks, vs, dos = ([x[i] for x in layers] for i in range(4))
     outs = [torch.full_like(q, float("nan")) for q in qs]
@@ -60,6 +67,11 @@ def test_stack_equals_single_layer_calls(case):
                              w.offsets, Hq, Hkv, D, w.scale, rev(dqs), rev(dks), rev(dvs), ws)
     dualkv.dualkv_check_status()
     for l in range(n):
+        # each layer of the stack against the fp64 oracle of that layer (its own window)
+        hq, hk, hv, hdo = host[l]
+        ref = oracle.dualkv(P, w.N, w.offsets, Hq, Hkv, D, w.scale, windows[l], hq, hk, hv, hdo)
+        got = dict(out=outs[l], lse=lses[l], dq=dqs[l], dk=dks[l], dv=dvs[l])
+        o_error_log(f"{name} layer {l} (window {windows[l]})", check_full(got, ref))
         out, lse = dualkv.forward(qs[l], ks[l], vs[l], P, w.offsets, windows[l], w.scale)
         dq, dk, dv = dualkv.backward(qs[l], ks[l], vs[l], out, lse, dos[l], P, w.offsets, windows[l], w.scale)
         for key, a, b in (("out", outs[l], out), ("lse", lses[l], lse), ("dq", dqs[l], dq), ("dk", dks[l], dk),

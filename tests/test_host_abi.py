@@ -107,9 +107,66 @@ def test_binding_refuses_cpu_tensors(lib):
         dualkv.dualkv_fwd(x, x, x, 2, 1, [0, 2], 2, 2, 64, 0.125, 0, x, torch.zeros(2, 4), None)
 
 
+def test_binding_checks_shapes_before_the_c_call(lib):
+    # meta tensors carry shapes and dtypes but no memory: a shape that does not fit the
+    # layout (T = P + R_offsets[N] rows) is refused before any pointer is passed on
+    import torch
+    P, off, Hq, Hkv, D = 6, [0, 3, 5], 4, 2, 64
+    T = P + off[-1]
+
+    def t(*shape, dt=torch.bfloat16):
+        return torch.empty(*shape, dtype=dt, device="meta")
+
+    q, kv, lse = t(T, Hq, D), t(T, Hkv, D), t(Hq, T, dt=torch.float32)
+    bad = {"q": t(T - 1, Hq, D), "k": t(T, Hq, D), "v": t(T, Hkv, D // 2), "out": t(T, Hq * D), "lse": t(T, Hq)}
+    args = dict(q=q, k=kv, v=kv, out=q, lse=lse)
+    for name, b in bad.items():
+        a = dict(args, **{name: b})
+        with pytest.raises(ValueError, match="shape"):
+            dualkv.dualkv_fwd(a["q"], a["k"], a["v"], P, 2, off, Hq, Hkv, D, 0.125, 0, a["out"], a["lse"])
+    with pytest.raises(ValueError, match="shape"):
+        dualkv.dualkv_bwd(q, kv, kv, q, lse, q, P, 2, off, Hq, Hkv, D, 0.125, 0, q, t(T + 1, Hkv, D), kv, None, 0)
+    with pytest.raises(ValueError, match="shape"):
+        dualkv.dualkv_bwd_noalloc(q, kv, kv, q, lse, t(T, Hq, 2 * D), P, 2, off, Hq, Hkv, D, 0.125, 0, q, kv, kv)
+    with pytest.raises(ValueError, match="shape"):
+        dualkv.dualkv_fwd_layers([q, q], [kv, kv], [kv, t(1, Hkv, D)], [0, 0], P, 2, off, Hq, Hkv, D, 0.125, [q, q],
+                                 [lse, lse])
+    with pytest.raises(ValueError, match="R_offsets"):
+        dualkv.dualkv_fwd(q, kv, kv, P, 3, off, Hq, Hkv, D, 0.125, 0, q, lse)
+    # right shapes: refused next for not being CUDA tensors, still before the C call
+    with pytest.raises(ValueError, match="CUDA"):
+        dualkv.dualkv_fwd(q, kv, kv, P, 2, off, Hq, Hkv, D, 0.125, 0, q, lse)
+
+
+def test_noalloc_refuses_head_dim_512_before_any_device_work(lib):
+    off = (ctypes.c_int32 * 2)(0, 2)
+    p = ctypes.c_void_p(0x10000)
+    assert lib.dualkv_bwd_noalloc(p, p, p, p, p, p, 4, 1, off, 4, 2, 512, 0.125, 0, p, p, p, None) == \
+        dualkv.DUALKV_ERR_UNSUPPORTED
+    assert lib.dualkv_bwd_noalloc(p, p, p, p, p, p, 4, 1, off, 4, 2, 96, 0.125, 0, p, p, p, None) == \
+        dualkv.DUALKV_ERR_INVALID
+
+
 def test_selftest_rejects_out_of_range_limit(lib):
     assert lib.dualkv_selftest_timeout(10, None) == dualkv.DUALKV_ERR_INVALID
     assert lib.dualkv_selftest_timeout(100 * 10**9, None) == dualkv.DUALKV_ERR_INVALID
+    assert lib.dualkv_selftest_kernel(0, 10, None) == dualkv.DUALKV_ERR_INVALID
+    assert lib.dualkv_selftest_kernel(3, 50_000_000, None) == dualkv.DUALKV_ERR_INVALID
+    assert lib.dualkv_selftest_kernel(-1, 50_000_000, None) == dualkv.DUALKV_ERR_INVALID
+
+
+def test_plan_cache_evicts_least_recently_used(tmp_path):
+    # the cache class is host-only C++: compile a small driver against it and run it
+    import shutil
+    import subprocess
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if cxx is None:
+        pytest.skip("no C++ compiler")
+    exe = str(tmp_path / "lru")
+    subprocess.run([cxx, "-std=c++17", "-O1", "-Wall", "-I", os.path.join(ROOT, "shared_prompt_exact_gb300", "csrc"),
+                    os.path.join(ROOT, "tests", "plan_cache_lru.cpp"), "-o", exe], check=True)
+    res = subprocess.run([exe], capture_output=True, text=True)
+    assert res.returncode == 0 and res.stdout.strip() == "ok", res.stdout + res.stderr
 
 
 def test_head_range_validation_before_any_device_work(lib):
