@@ -42,8 +42,14 @@ from shared_prompt_exact_gb300 import workloads as wl  # noqa: E402
 METRIC = "DualKV attn fwd+bwd useful TFLOP/s & % BF16 tensor peak, N=32 P=6144 R=2048"
 UNIT = "TFLOP/s"
 
-# algorithmic tensor-core FLOPs per attended pair per head (x D) of each kernel
+# algorithmic tensor-core FLOPs per attended pair per head (x D) of each kernel kind:
+# forward S and PV; dK/dV recomputes S and dP and forms dV and dK; dQ recomputes S
+# and dP and forms dQ
 KERNEL_FLOPS_PER_PAIR = {"fwd": 4, "dkv": 8, "dq": 6}
+
+
+def kernel_flops_per_pair(kind, D):
+    return KERNEL_FLOPS_PER_PAIR.get(kind)
 
 
 # ------------------------------------------------------------------ helpers
@@ -69,7 +75,7 @@ def peaks():
 
 # source files each timed kernel kind is built from (its kernel, the shared device
 # helpers, the work-list planner and the launch code)
-_COMMON_SOURCES = ["ptx.cuh", "kernels.h", "plan.h", "plan.cpp", "api.cu"]
+_COMMON_SOURCES = ["ptx.cuh", "checks.cuh", "kernels.h", "plan.h", "plan.cpp", "api.cu"]
 KERNEL_SOURCES = {"fwd": ["fwd.cu"] + _COMMON_SOURCES, "dkv": ["bwd.cu"] + _COMMON_SOURCES,
                   "dq": ["bwd.cu"] + _COMMON_SOURCES}
 
@@ -329,6 +335,139 @@ def measure_packing(w, dev, stream, reps):
     return res
 
 
+# ------------------------------------------------------------------ other workloads, fresh layouts
+def _timed_on(stream, dev, fn, reps):
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / reps
+
+
+def measure_workload(name, dev, stream, steps, sampler):
+    """fwd, bwd and fwd+bwd useful TFLOP/s of one workload (its own seeded inputs,
+    resident in HBM) and the per-kernel times of its launches; each timed alone with
+    CUDA events on the launching stream after two warm-up steps."""
+    from shared_prompt_exact_gb300 import dualkv
+    w = wl.WORKLOADS[name]
+    q, k, v, do = (x.to(dev) for x in wl.draw_inputs(w))
+    out = torch.empty_like(q)
+    lse = torch.empty(w.Hq, w.T, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = dualkv.workspace_for(w.P, w.offsets, w.Hq, w.Hkv, w.D, w.window, dev)
+
+    def fwd():
+        dualkv.dualkv_fwd(q, k, v, w.P, w.N, w.offsets, w.Hq, w.Hkv, w.D, w.scale, w.window, out, lse, stream)
+
+    def bwd():
+        dualkv.dualkv_bwd(q, k, v, out, lse, do, w.P, w.N, w.offsets, w.Hq, w.Hkv, w.D, w.scale, w.window, dq, dk,
+                          dv, ws, None, stream)
+
+    def step():
+        fwd()
+        bwd()
+
+    for _ in range(2):
+        step()
+    dualkv.dualkv_check_status(stream)
+    t0 = time.time()
+    ms_step = _timed_on(stream, dev, step, steps)
+    t1 = time.time()
+    ms_fwd = _timed_on(stream, dev, fwd, steps)
+    ms_bwd = _timed_on(stream, dev, bwd, steps)
+    dualkv.dualkv_profile_read()
+    dualkv.dualkv_profile_enable(True)
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(dev)
+    kt = dualkv.dualkv_profile_read()
+    dualkv.dualkv_profile_enable(False)
+    dualkv.dualkv_check_status(stream)
+    pairs = layout_pairs(w)
+    f_fwd, f_bwd = useful_flops(pairs, w.D, w.Hq)
+    pk = peaks()
+    res = {
+        "P": w.P, "N": w.N, "R": (w.R[0] if len(set(w.R)) == 1 else "ragged"), "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+        "window": w.window, "pairs_per_head": pairs, "rho": dualkv.dualkv_rho(w.P, w.N, w.offsets),
+        "fwd": {"ms": ms_fwd, "tflops": f_fwd / (ms_fwd * 1e-3) / 1e12},
+        "bwd": {"ms": ms_bwd, "tflops": f_bwd / (ms_bwd * 1e-3) / 1e12},
+        "fwd_bwd": {"ms": ms_step, "tflops": (f_fwd + f_bwd) / (ms_step * 1e-3) / 1e12},
+        "kernels_ms_per_step": {kk: ms / 2 for kk, (ms, n) in kt.items() if n},
+        "clocks": sampler.summary(t0, t1),
+    }
+    res["pct_bf16_peak"] = {"measured_burst": res["fwd_bwd"]["tflops"] / pk["bf16_burst"],
+                            "measured_sustained": res["fwd_bwd"]["tflops"] / pk["bf16_sustained"],
+                            "nominal_2250": res["fwd_bwd"]["tflops"] / 2250.0}
+    del q, k, v, do, out, lse, dq, dk, dv, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def fresh_r_lists(n, N=32, lo=256, hi=4096, seed=20260518):
+    """Per-step ragged response lengths, uniform on [lo, hi], one fixed-seed draw per step."""
+    import numpy as np
+    return [[int(x) for x in np.random.default_rng(seed + 1000 + i).integers(lo, hi + 1, N)] for i in range(n)]
+
+
+def measure_fresh_layouts(base, dev, stream, steps):
+    """The DAPO-like workload with a new ragged response list every step (a training
+    loop repacks each micro-batch, so every call meets a layout it has not planned):
+    plan building, its upload and the step all inside the timed region.  Compared
+    with the same steps repeated on one layout (plans cached)."""
+    from shared_prompt_exact_gb300 import dualkv
+    lists = fresh_r_lists(steps, N=base.N)
+    ws_ = [wl.custom(base.P, R, base.Hq, base.Hkv, base.D, base.window, seed=base.seed) for R in lists]
+    Tmax = max(x.T for x in ws_)
+    gen = torch.Generator(device=dev).manual_seed(base.seed)
+    rnd = lambda *shape: torch.randn(*shape, generator=gen, device=dev).to(torch.bfloat16)  # noqa: E731
+    q, k, v, do = rnd(Tmax, base.Hq, base.D), rnd(Tmax, base.Hkv, base.D), rnd(Tmax, base.Hkv, base.D), \
+        rnd(Tmax, base.Hq, base.D)
+    out = torch.empty_like(q)
+    lse_all = torch.empty(base.Hq * Tmax, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = max(dualkv.dualkv_bwd_workspace_bytes(x.P, x.N, x.offsets, x.Hq, x.Hkv, x.D, x.window) for x in ws_)
+    wsb = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+
+    def step(x):
+        T = x.T
+        lse = lse_all[: x.Hq * T].view(x.Hq, T)
+        dualkv.dualkv_fwd(q[:T], k[:T], v[:T], x.P, x.N, x.offsets, x.Hq, x.Hkv, x.D, x.scale, x.window, out[:T], lse,
+                          stream)
+        dualkv.dualkv_bwd(q[:T], k[:T], v[:T], out[:T], lse, do[:T], x.P, x.N, x.offsets, x.Hq, x.Hkv, x.D, x.scale,
+                          x.window, dq[:T], dk[:T], dv[:T], wsb, None, stream)
+
+    flops = sum(sum(useful_flops(layout_pairs(x), x.D, x.Hq)) for x in ws_)
+    # fresh: drop every plan, warm up on three other layouts, then a layout not seen
+    # before on each timed step
+    warm = [wl.custom(base.P, R, base.Hq, base.Hkv, base.D, base.window, seed=base.seed)
+            for R in fresh_r_lists(3, N=base.N, seed=base.seed + 777)]
+    torch.cuda.synchronize(dev)
+    dualkv.dualkv_release()
+    for x in warm:
+        step(x)
+    it = iter(ws_)
+    ms_fresh = _timed_on(stream, dev, lambda: step(next(it)), steps)
+    # cached: the same sequence of layouts again, every plan now resident
+    it = iter(ws_)
+    ms_cached = _timed_on(stream, dev, lambda: step(next(it)), steps)
+    dualkv.dualkv_check_status(stream)
+    tf_fresh = flops / (ms_fresh * steps * 1e-3) / 1e12
+    tf_cached = flops / (ms_cached * steps * 1e-3) / 1e12
+    n_plans, cache_bytes = dualkv.dualkv_plan_cache_info()
+    del q, k, v, do, out, lse_all, dq, dk, dv, wsb
+    torch.cuda.empty_cache()
+    return {"workload": f"{base.name} with a new R list each step (uniform [256, 4096], N={base.N})",
+            "steps": steps, "ms_per_step_fresh": ms_fresh, "tflops_fresh": tf_fresh,
+            "ms_per_step_cached": ms_cached, "tflops_cached": tf_cached,
+            "fresh_over_cached_tflops": tf_fresh / tf_cached,
+            "compared": "the same sequence of layouts, first unplanned, then with every plan cached",
+            "plan_cache": {"resident_plans": n_plans, "device_bytes": cache_bytes}}
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_dualkv(args, w):
     from shared_prompt_exact_gb300 import build as pbuild
@@ -432,14 +571,16 @@ def run_dualkv(args, w):
     dom = max(kt, key=lambda kk: kt[kk][0])
     pk = peaks()
     roofline = None
-    if dom in KERNEL_FLOPS_PER_PAIR and kt[dom][1] > 0:
-        per_launch_flops = KERNEL_FLOPS_PER_PAIR[dom] * D * Hq * pairs * head_frac
+    if kernel_flops_per_pair(dom, D) and kt[dom][1] > 0:
+        per_launch_flops = kernel_flops_per_pair(dom, D) * D * Hq * pairs * head_frac
         avg_ms = kt[dom][0] / kt[dom][1]
         achieved = per_launch_flops / (avg_ms * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": pk["bf16_sustained"],
-                    "unit": "TFLOP/s", "frac": achieved / pk["bf16_sustained"],
+        roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": pk["bf16_burst"],
+                    "unit": "TFLOP/s", "frac": achieved / pk["bf16_burst"],
                     "traffic": ncu_traffic(dom, w.name),
-                    "peak_source": pk["source"] + " bf16 sustained (kernel timed inside a multi-step loop)",
+                    "peak_source": pk["source"] + " bf16 burst (each launch lasts milliseconds, inside a step of "
+                                   "tens of milliseconds)",
+                    "frac_of_sustained": achieved / pk["bf16_sustained"],
                     "avg_launch_ms": avg_ms, "algorithmic_flops_per_launch": per_launch_flops}
     kernels = {kk: {"ms_per_launch": (ms / n if n else None), "launches": n} for kk, (ms, n) in kt.items()}
 
@@ -580,6 +721,17 @@ def run_dualkv(args, w):
     if not args.no_pack:
         packing = measure_packing(w, dev, stream, max(3, min(args.steps, 10)))
 
+    # every other workload of the benchmark's configuration list, measured the same way
+    others = {}
+    if not args.no_configs and not shard:
+        for name in ("qwen16", "dapo32", "gemma_global", "gemma_window"):
+            if name != w.name:
+                others[name] = measure_workload(name, dev, stream, max(3, min(args.steps, 5)), sampler)
+
+    fresh = None
+    if not args.no_fresh_layouts and not shard:
+        fresh = measure_fresh_layouts(wl.WORKLOADS["dapo32"], dev, stream, max(4, min(args.steps, 10)))
+
     sampler.stop()
     clocks = sampler.summary(t_start, t_end)
 
@@ -615,6 +767,8 @@ def run_dualkv(args, w):
             "replicated": replicated,
             "tensor_packing": packing,
             "head_groups": head_groups,
+            "other_workloads": others,
+            "fresh_layouts": fresh,
             "gpu_launches": int(round(launches_per_step * args.steps)),
             "clocks": clocks,
         }
@@ -731,6 +885,9 @@ def main(argv=None):
     ap.add_argument("--no-replicated", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pack", action="store_true", help="skip the pack/unpack/fold measurement")
+    ap.add_argument("--no-configs", action="store_true", help="skip the blocks of the other four workloads")
+    ap.add_argument("--no-fresh-layouts", action="store_true",
+                    help="skip the block with a new ragged layout every step")
     ap.add_argument("--shard", choices=("replicas", "heads"), default="replicas",
                     help="N > 1: independent replicas (weak scaling) or one micro-batch split by kv-head group "
                          "(strong scaling)")

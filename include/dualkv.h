@@ -301,9 +301,13 @@ int dualkv_selftest_timeout(uint64_t limit_ns, void* stream);
  *   which = 1  the dK/dV kernel; the first query block of its first CTA gets
  *              one barrier arrival too few, so the waits for it run out;
  *   which = 2  the forward kernel given a work list whose first entry lies past
- *              the last row; the kernel's range check skips it.
- * Each kernel records the failure in the status word, drains its copies and
- * tensor-core operations, frees its tensor memory and returns;
+ *              the last row; the kernel's range check skips it;
+ *   which = 3  the backward preprocess and dQ kernel given a dQ work list whose
+ *              first entry lies past the last row; the preprocess, which checks
+ *              that list before the dQ kernel reads it, empties the entry.
+ * The failure is recorded in the status word; a kernel whose wait ran out
+ * drains its copies and tensor-core operations, frees its tensor memory and
+ * returns;
  * dualkv_check_status() then reports DUALKV_ERR_DEVICE and the context stays
  * usable.  The call allocates and frees its own small buffers and returns
  * after the kernel has finished on `stream`: DUALKV_OK, DUALKV_ERR_INVALID

@@ -527,6 +527,12 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
   const int gs = Hq / Hkv;
   PrepArgs pa{static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, delta, lse2, T, Hq, D,
               kv_lo * gs, kv_hi * gs};
+  if (D != 512) {  // the dQ kernel's work list is checked by the preprocess
+    pa.check_items = pl->dq_items;
+    pa.n_check = pl->n_dq;
+    pa.check_tile = dq_query_tile(D);
+    pa.status = status;
+  }
   if (timed(DUALKV_KERNEL_PREP, st, [&] { return launch_prep(pa, st); }) != cudaSuccess) return DUALKV_ERR_CUDA;
 
   if (D == 512) {
@@ -802,7 +808,7 @@ int dualkv_plan_cache_info(int* n_plans, int64_t* device_bytes) {
 }
 
 int dualkv_selftest_kernel(int which, uint64_t limit_ns, void* stream) {
-  if (which < 0 || which > 2) return DUALKV_ERR_INVALID;
+  if (which < 0 || which > 3) return DUALKV_ERR_INVALID;
   if (limit_ns < 1000000ull || limit_ns > 10000000000ull) return DUALKV_ERR_INVALID;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   std::lock_guard<std::mutex> lock(g_mu);
@@ -818,12 +824,13 @@ int dualkv_selftest_kernel(int which, uint64_t limit_ns, void* stream) {
   constexpr int64_t T = P + 256;
   const float scale = 0.08838834764831845f;
   DevPlan* pl = nullptr;
-  if ((rc = get_plan(P, N, off, Hq, Hkv, D, 0, 0, Hkv, which == 1, st, &pl))) return rc;
+  if ((rc = get_plan(P, N, off, Hq, Hkv, D, 0, 0, Hkv, which == 1 || which == 3, st, &pl))) return rc;
   const size_t tensor_bytes = (size_t)T * Hq * D * 2;
   const WsLayout ws = ws_layout(T, Hq, D, pl->nslots, 0);
   uint8_t* mem = nullptr;
   const size_t o_lse = 7 * tensor_bytes, o_ws = align256(o_lse + sizeof(float) * Hq * T),
-               o_items = o_ws + align256(ws.total), total = o_items + align256(sizeof(QTileItem) * pl->n_fwd);
+               o_items = o_ws + align256(ws.total),
+               total = o_items + align256(sizeof(QTileItem) * (pl->n_fwd > pl->n_dq ? pl->n_fwd : pl->n_dq));
   if (cudaMalloc(&mem, total) != cudaSuccess) return DUALKV_ERR_CUDA;
   auto done = [&](int code) {
     cudaStreamSynchronize(st);
@@ -836,6 +843,34 @@ int dualkv_selftest_kernel(int which, uint64_t limit_ns, void* stream) {
   float* lse = reinterpret_cast<float*>(mem + o_lse);
   uint8_t* wsb = mem + o_ws;
   CUtensorMap tq, tk, tv, tdo;
+  if (which == 3) {
+    // dQ: its work list's first entry moved past the last row; the preprocess, which
+    // checks the list before the dQ kernel reads it, empties the entry
+    Layout L{P, N, std::vector<int32_t>(off, off + N + 1), Hq, Hkv, D, 0};
+    std::vector<QTileItem> bad = plan_qtiles(L, dq_query_tile(D), dq_key_tile(D));
+    bad[0].q_row0 = (int32_t)T + 64;
+    QTileItem* d_items = reinterpret_cast<QTileItem*>(mem + o_items);
+    if (cudaMemcpyAsync(d_items, bad.data(), sizeof(QTileItem) * bad.size(), cudaMemcpyHostToDevice, st) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return done(DUALKV_ERR_CUDA);
+    float* delta = reinterpret_cast<float*>(wsb + ws.delta);
+    float* lse2 = reinterpret_cast<float*>(wsb + ws.lse2);
+    PrepArgs pa{static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, delta, lse2, T,
+                Hq, D};
+    pa.check_items = d_items;
+    pa.n_check = (int)bad.size();
+    pa.check_tile = dq_query_tile(D);
+    pa.status = status;
+    if (launch_prep(pa, st) != cudaSuccess) return done(DUALKV_ERR_CUDA);
+    if (make_tmap(&tq, q, T, Hq, D, dq_query_tile(D)) || make_tmap(&tk, k, T, Hkv, D, dq_key_tile(D)) ||
+        make_tmap(&tv, v, T, Hkv, D, dq_key_tile(D)) || make_tmap(&tdo, dout, T, Hq, D, dq_query_tile(D)))
+      return done(DUALKV_ERR_CUDA);
+    DqArgs qa{d_items, delta, lse2, static_cast<__nv_bfloat16*>(dk), (int)T, Hq, Hkv, 0,
+              scale * 1.4426950408889634f, scale, status};
+    if (launch_dq(D, tq, tk, tv, tdo, qa, (int)bad.size(), st) != cudaSuccess) return done(DUALKV_ERR_CUDA);
+    return done(mark_use(&pl->last_use, st));
+  }
   if (which != 1) {
     // forward: every CTA waits for K/V unit 0, which is never loaded (which = 0), or the
     // first work item is moved past the last row (which = 2)

@@ -30,8 +30,30 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- prep
 // Delta[h, t] = sum_d dO[t,h,d] * O[t,h,d];  lse2[h, t] = lse[h, t] * log2(e)
+// The dQ kernel's work list is checked here, in the launch that always precedes it:
+// an entry whose rows, head or key tiles fall outside the tensors is recorded as a
+// bounds error and replaced by an empty item (no key tiles, no rows), which the dQ
+// kernel skips without any access.
+__device__ __forceinline__ void sanitize_items(const PrepArgs& a) {
+  if (!a.check_items) return;
+  const int64_t nthreads = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < a.n_check; i += nthreads) {
+    QTileItem it = a.check_items[i];
+    if (!qtile_ok(it, a.T, a.Hq, a.check_tile, a.check_tile)) {
+      if (a.status) atomicOr(a.status, kDevErrBounds);
+      it.q_row0 = 0;
+      it.q_rows = 0;
+      it.head = 0;
+      it.reg[0] = KeyRegion{0, 0, 0, 0, 0};
+      it.reg[1] = KeyRegion{0, 0, 0, 0, 0};
+      a.check_items[i] = it;
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(256) prep_kernel(const PrepArgs a) {
+  sanitize_items(a);
   constexpr int LPR = (D / 8) < 32 ? (D / 8) : 32;  // lanes per row
   constexpr int PASSES = D / (8 * LPR);
   constexpr int RPW = 32 / LPR;                       // rows per warp
@@ -169,10 +191,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
 
   const uint32_t warp = warp_id(), lane = lane_id();
   FailState fs{&ctl.abort_flag, a.status};
-  // key tiles of an item, or -1 for an item outside the tensors: every role skips it
-  // (nothing is read or written for it) and one thread records the violation
-  auto tiles_of = [&](const QTileItem& q) {
-    if (!qtile_ok(q, a.T, a.Hq, C::BM, C::BN)) return -1;
+  auto tiles_of = [](const QTileItem& q) {
     return (q.reg[0].t_hi - q.reg[0].t_lo) + (q.reg[1].t_hi - q.reg[1].t_lo);
   };
 
@@ -220,7 +239,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
       for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
         const QTileItem it = a.items[item];
         const int nt = tiles_of(it);
-        if (nt <= 0) continue;
+        if (nt == 0) continue;
         const int kvh = it.head / (a.Hq / a.Hkv);
         // Q / dO are overwritten only after every GEMM of the previous item has completed
         if (kx > 0 && !(ok = mbar_wait(&ctl.q_free, (kx - 1) & 1, fs))) break;
@@ -273,7 +292,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     int g = 0, kx = 0;
     for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
       const int nt = tiles_of(a.items[item]);
-      if (nt <= 0) continue;
+      if (nt == 0) continue;
       // Q copied into TMEM (after its TMA load, which also brought dO)
       if (!(ok = mbar_wait(&ctl.q_tmem, kx & 1, fs))) break;
       ++kx;
@@ -324,7 +343,7 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     int g = 0, kx = 0;
     for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
       const int nt = tiles_of(a.items[item]);
-      if (nt <= 0) continue;
+      if (nt == 0) continue;
       for (int j = 0; j < nt && ok; ++j, ++g) {
         const int ks = g % C::NSK;
         if (!(ok = mbar_wait(&ctl.ds_full, g & 1, fs))) break;
@@ -360,10 +379,6 @@ __global__ void __launch_bounds__(DqCfg<D>::THREADS, 1)
     for (int item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
       const QTileItem it = a.items[item];
       const int nt = tiles_of(it);
-      if (nt < 0) {
-        if (warp == 2 && lane == 0 && a.status) atomicOr(a.status, kDevErrBounds);
-        continue;
-      }
       const int qpos = it.q_pos0 + row;
       const bool valid = row < it.q_rows;
       // this warp writes dQ columns [grp * D / NG, (grp + 1) * D / NG) of its row

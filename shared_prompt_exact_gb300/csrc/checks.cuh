@@ -20,9 +20,9 @@ __device__ __forceinline__ bool rows_ok(int64_t row0, int64_t rows, int64_t T, i
 // [t_lo, t_hi) lies inside ceil(count / key_tile) tiles.
 __device__ __forceinline__ bool region_ok(const KeyRegion& r, int64_t T, int key_tile) {
   if (r.t_lo == r.t_hi) return r.t_lo >= 0;
-  const int64_t ntiles = ((int64_t)r.count + key_tile - 1) / key_tile;
+  // t_hi <= ceil(count / key_tile), without a division
   return r.row0 >= 0 && r.count >= 0 && (int64_t)r.row0 + r.count <= T && r.t_lo >= 0 && r.t_lo < r.t_hi &&
-         r.t_hi <= ntiles;
+         (int64_t)(r.t_hi - 1) * key_tile < (int64_t)r.count;
 }
 
 // A forward / dQ / D = 512 block work item: query tile of at most tile_rows rows of

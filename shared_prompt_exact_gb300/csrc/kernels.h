@@ -40,6 +40,11 @@ struct PrepArgs {
   int64_t T;
   int Hq, D;
   int h_lo = 0, h_hi = -1;  // q-heads [h_lo, h_hi) are prepared (h_hi < 0: all)
+  // the dQ work list to check (and to empty any entry outside the tensors) before the
+  // dQ kernel runs; null: none
+  QTileItem* check_items = nullptr;
+  int n_check = 0, check_tile = 128;
+  uint32_t* status = nullptr;
 };
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st);
 

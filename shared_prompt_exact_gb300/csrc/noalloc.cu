@@ -148,6 +148,10 @@ extern "C" int dualkv_bwd_noalloc(const void* q, const void* k, const void* v, c
   const float sl2 = scale * 1.4426950408889634f;
 
   PrepArgs pa{static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, delta, lse2, T, Hq, D};
+  pa.check_items = reinterpret_cast<QTileItem*>(base + o_dq);  // checked before the dQ kernel reads it
+  pa.n_check = (int)dq_items.size();
+  pa.check_tile = dq_query_tile(D);
+  pa.status = status;
   if (launch_prep(pa, st) != cudaSuccess) return fail(DUALKV_ERR_CUDA);
   CUtensorMap tq, tk, tv, tdo;
   if (tmap(&tq, q, T, Hq, D, dkv_query_block(D)) || tmap(&tk, k, T, Hkv, D, dkv_key_tile(D)) ||

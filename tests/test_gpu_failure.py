@@ -35,10 +35,11 @@ KERNEL_CASES = [
     (0, "forward: a K/V tile never loaded"),
     (1, "dK/dV: a query block one barrier arrival short"),
     (2, "forward: a work item past the last row"),
+    (3, "dQ: a work item past the last row, emptied by the preprocess"),
 ]
 
 
-@pytest.mark.parametrize("which,what", KERNEL_CASES, ids=["fwd-timeout", "dkv-timeout", "fwd-bounds"])
+@pytest.mark.parametrize("which,what", KERNEL_CASES, ids=["fwd-timeout", "dkv-timeout", "fwd-bounds", "dq-bounds"])
 def test_production_kernel_failure_paths(which, what):
     # the real kernels' failure handling: the bounded waits (50 ms here) run out, or
     # the range check skips the bad entry; the kernel drains, frees its tensor memory
