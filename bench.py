@@ -374,8 +374,11 @@ def measure_workload(name, dev, stream, steps, sampler):
     for _ in range(2):
         step()
     dualkv.dualkv_check_status(stream)
+    # enough steps for the timed region to last about 0.6 s, so that the clock sampler
+    # (every 200 ms) sees it
+    reps = max(steps, min(200, int(math.ceil(600.0 / max(_timed_on(stream, dev, step, 1), 1e-3)))))
     t0 = time.time()
-    ms_step = _timed_on(stream, dev, step, steps)
+    ms_step = _timed_on(stream, dev, step, reps)
     t1 = time.time()
     ms_fwd = _timed_on(stream, dev, fwd, steps)
     ms_bwd = _timed_on(stream, dev, bwd, steps)
@@ -393,6 +396,7 @@ def measure_workload(name, dev, stream, steps, sampler):
     res = {
         "P": w.P, "N": w.N, "R": (w.R[0] if len(set(w.R)) == 1 else "ragged"), "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
         "window": w.window, "pairs_per_head": pairs, "rho": dualkv.dualkv_rho(w.P, w.N, w.offsets),
+        "timed_steps": reps,
         "fwd": {"ms": ms_fwd, "tflops": f_fwd / (ms_fwd * 1e-3) / 1e12},
         "bwd": {"ms": ms_bwd, "tflops": f_bwd / (ms_bwd * 1e-3) / 1e12},
         "fwd_bwd": {"ms": ms_step, "tflops": (f_fwd + f_bwd) / (ms_step * 1e-3) / 1e12},
