@@ -545,8 +545,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
         make_block_tmap(&tP64, pblk, pl->n_blocks, 64) || make_block_tmap(&tDS64, dsblk, pl->n_blocks, 64) ||
         make_block_tmap(&tDS128, dsblk, pl->n_blocks, 128))
       return DUALKV_ERR_CUDA;
-    PdsArgs p0{pl->dq_items, pl->block_base, lse2, delta, nullptr, pblk, (int)T, Hq, Hkv, W, sl2, status, pl->n_blocks};
-    PdsArgs p1{pl->dq_items, pl->block_base, lse2, delta, pblk, dsblk, (int)T, Hq, Hkv, W, sl2, status, pl->n_blocks};
+    PdsArgs pa5{pl->dq_items, pl->block_base, lse2, delta, pblk, dsblk, (int)T, Hq, Hkv, W, sl2, status,
+                pl->n_blocks};
     XtgArgs xv{pl->xt_items, pl->xt_entries, static_cast<__nv_bfloat16*>(dv), partial, 1, (int)T, Hq, Hkv, 1.f, status,
                pl->n_xt_entries, pl->n_blocks, pl->nslots};
     XtgArgs xk{pl->xt_items, pl->xt_entries, static_cast<__nv_bfloat16*>(dk), partial, 0, (int)T, Hq, Hkv, scale, status,
@@ -554,8 +554,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
     Dq512Args qa{pl->dq_items, pl->block_base, static_cast<__nv_bfloat16*>(dq), (int)T, Hq, Hkv, scale, status,
                  pl->n_blocks};
     if (timed(DUALKV_KERNEL_DKV, st, [&] {
-          cudaError_t e = launch_pds(0, tq, tk, p0, pl->n_dq, st);
-          if (e == cudaSuccess) e = launch_pds(1, tdo, tv, p1, pl->n_dq, st);
+          const bool pair_heads = (Hq / Hkv) % 2 == 0 && pl->n_dq % 2 == 0;
+          cudaError_t e = launch_pds_fused(tq, tdo, tk, tv, pa5, pl->n_dq, pair_heads, st);
           if (e == cudaSuccess) e = launch_xtg(tP64, tdo64, xv, pl->n_xt, st);
           if (e == cudaSuccess) e = launch_xtg(tDS64, tq64, xk, pl->n_xt, st);
           return e;

@@ -5,8 +5,8 @@
 // of bwd.cu do not fit.  This backward materialises the two 128 x 128 bf16
 // blocks of every (query tile, key tile) pair the walk visits, then reduces
 // them with plain tensor-core GEMMs -- no product is computed twice:
-//   pds<0>:  S = Q K^T  ->  P  = exp(S - LSE)           (masked, bf16 block)
-//   pds<1>:  dP = dO V^T -> dS = P (dP - Delta)         (bf16 block)
+//   pds:     S = Q K^T  ->  P  = exp(S - LSE)           (masked, bf16 block)
+//            dP = dO V^T -> dS = P (dP - Delta)         (bf16 block, P from registers)
 //   xtg:     dV = sum P^T dO,  dK = scale sum dS^T Q    (per key tile; fixed order)
 //   dq512:   dQ = scale sum dS K                        (per query tile)
 // The formulas are the analytic backward of softmax attention; the fold of
@@ -36,70 +36,103 @@ __device__ __forceinline__ void walk_tile(const QTileItem& it, int j, int& r, in
   }
 }
 
-// ---------------------------------------------------------------- P / dS blocks
-// The resident operand (Q or dO, 128 rows x 512) is an A operand in TMEM: it
-// lands by TMA in the ring's shared memory, the compute warps copy it into
-// TMEM, and the ring then streams K / V tiles.  Only B is read from shared
-// memory by the MMAs, and the ring is 7 units deep.
-struct PdsCfg {
+// Warps 2-9 convert S and dP: warps w and w+4 share TMEM lane quarter w % 4 (one
+// query row per thread) and take key columns [0, 64) and [64, 128) of each block.
+constexpr int kPdsThreads = 320;
+
+// ---------------------------------------------------------------- P and dS blocks in one pass
+// One CTA per query tile (128 rows x q-head) forms, for every key tile it visits,
+// both S = Q K^T and dP = dO V^T and writes both bf16 blocks, P = exp(S - LSE)
+// and dS = P (dP - Delta), keeping P on chip in between.  Q is the A operand of S
+// from TMEM (256 columns), dO the A operand of dP from shared memory (resident,
+// 128 KB), and K / V tiles stream through a 3-unit ring; S and dP have one TMEM
+// buffer each (128 columns): each block's two GEMMs keep the pipe busy while the
+// compute warps drain the other one.
+//
+// CS = 2: the two CTAs of a cluster take the same query rows for two q-heads of
+// one kv-head group, so they walk the same K / V tiles.  Each unit of the ring
+// then arrives by one multicast load per CTA (one 64-column chunk each, delivered
+// to both), which halves the L2 -> SM traffic of the walk; a slot is refilled once
+// the MMAs of both CTAs have read it (each commits to both CTAs' empty barrier).
+struct PdsFCfg {
   static constexpr int BM = 128, BN = 128;
-  static constexpr int QCH = kD / 64;          // chunks of the resident operand
+  static constexpr int QCH = kD / 64;              // 64-column chunks of Q / dO / K / V
   static constexpr int UNIT_BYTES = 2 * BN * 128;  // two 64-column chunks of a key tile
-  static constexpr int KU = QCH / 2;           // units per key tile
-  static constexpr int A_BYTES = BM * kD * 2;  // 128 KB, staged in the ring before the first key tile
-  static constexpr int NST = 7;
-  static_assert(A_BYTES <= NST * UNIT_BYTES, "A is staged in the ring");
-  static constexpr int SMEM_BYTES = NST * UNIT_BYTES + 1024;
-  static constexpr uint32_t TM_A = 2 * BN;     // after the two S buffers: kD / 2 columns
-  static constexpr uint32_t TM_COLS = 512;
+  static constexpr int KU = QCH / 2;               // units per K or V tile
+  static constexpr int A_BYTES = BM * kD * 2;      // 128 KB: dO resident (Q staged here first)
+  static constexpr int NST = 3;
+  static constexpr int OFF_A = 0, OFF_RING = A_BYTES;
+  static constexpr int SMEM_BYTES = OFF_RING + NST * UNIT_BYTES + 1024;
+  static constexpr uint32_t TM_S = 0, TM_DP = BN, TM_Q = 2 * BN, TM_COLS = 512;
 };
 
-struct PdsCtl {
-  uint64_t a_full, a_tmem;
-  uint64_t ring_full[7], ring_empty[7];
-  uint64_t s_full[2], s_empty[2];
+struct PdsFCtl {
+  uint64_t q_full, q_tmem, do_full;
+  uint64_t ring_full[3], ring_empty[3];
+  uint64_t s_full, s_empty, dp_full, dp_empty;
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
 };
 
-// MODE 0: A = Q, B = K, writes P blocks.  MODE 1: A = dO, B = V, reads P, writes dS blocks.
-// Warps 2-9 convert S: warps w and w+4 share TMEM lane quarter w % 4 (one query
-// row per thread) and take key columns [0, 64) and [64, 128) of each block.
-constexpr int kPdsThreads = 320;
-template <int MODE>
+__device__ __forceinline__ bool same_walk(const QTileItem& x, const QTileItem& y) {
+  bool eq = x.q_row0 == y.q_row0 && x.q_pos0 == y.q_pos0 && x.q_rows == y.q_rows;
+#pragma unroll
+  for (int r = 0; r < 2; ++r)
+    eq = eq && x.reg[r].row0 == y.reg[r].row0 && x.reg[r].pos0 == y.reg[r].pos0 && x.reg[r].count == y.reg[r].count &&
+         x.reg[r].t_lo == y.reg[r].t_lo && x.reg[r].t_hi == y.reg[r].t_hi;
+  return eq;
+}
+
+template <int CS>
 __global__ void __launch_bounds__(kPdsThreads, 1)
-    pds_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const PdsArgs a) {
-  using C = PdsCfg;
+    pds_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const PdsArgs a) {
+  static_assert(CS == 1 || CS == 2, "one CTA, or a pair sharing the K / V walk");
+  using C = PdsFCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ PdsCtl ctl;
-  uint8_t* sRing = smem;
-  uint8_t* sA = smem;  // staging of the resident operand, before the ring is used
+  __shared__ PdsFCtl ctl;
+  uint8_t* sA = smem + C::OFF_A;  // Q staging, then dO
+  uint8_t* sRing = smem + C::OFF_RING;
 
   const QTileItem it = a.items[blockIdx.x];
   const int blk0 = a.block_base[blockIdx.x];
   const int nt_all = (it.reg[0].t_hi - it.reg[0].t_lo) + (it.reg[1].t_hi - it.reg[1].t_lo);
   // an item outside the tensors or naming blocks past the block array does nothing
-  const bool item_ok = qtile_ok(it, a.T, a.Hq, C::BM, C::BN) && blk0 >= 0 && (int64_t)blk0 + nt_all <= a.n_blocks;
+  bool item_ok = qtile_ok(it, a.T, a.Hq, C::BM, C::BN) && blk0 >= 0 && (int64_t)blk0 + nt_all <= a.n_blocks;
+  const int gsz = a.Hq / a.Hkv;
+  const int kvh = it.head / gsz;
+  uint32_t crank = 0;
+  if (CS == 2) {
+    // both CTAs of the pair take the same decision: both items valid and walking the
+    // same key tiles of one kv-head
+    crank = cluster_ctarank();
+    const QTileItem pit = a.items[blockIdx.x ^ 1u];
+    const int pblk0 = a.block_base[blockIdx.x ^ 1u];
+    const int pnt = (pit.reg[0].t_hi - pit.reg[0].t_lo) + (pit.reg[1].t_hi - pit.reg[1].t_lo);
+    const bool pok = qtile_ok(pit, a.T, a.Hq, C::BM, C::BN) && pblk0 >= 0 && (int64_t)pblk0 + pnt <= a.n_blocks;
+    item_ok = item_ok && pok && same_walk(it, pit) && pit.head / gsz == kvh;
+  }
   const int nt = item_ok ? nt_all : 0;
-  const int kvh = it.head / (a.Hq / a.Hkv);
   const uint32_t warp = warp_id(), lane = lane_id();
   FailState fs{&ctl.abort_flag, a.status};
 
   if (threadIdx.x == 0) {
     if (!item_ok && a.status) atomicOr(a.status, kDevErrBounds);
     ctl.abort_flag = 0;
-    mbar_init(&ctl.a_full, 1);
-    mbar_init(&ctl.a_tmem, 8);
+    mbar_init(&ctl.q_full, 1);
+    mbar_init(&ctl.q_tmem, 8);
+    mbar_init(&ctl.do_full, 1);
     for (int i = 0; i < C::NST; ++i) {
       mbar_init(&ctl.ring_full[i], 1);
-      mbar_init(&ctl.ring_empty[i], 1);
+      mbar_init(&ctl.ring_empty[i], CS);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&ctl.s_full[i], 1);
-      mbar_init(&ctl.s_empty[i], 8);
-    }
+    mbar_init(&ctl.s_full, 1);
+    mbar_init(&ctl.s_empty, 8);
+    mbar_init(&ctl.dp_full, 1);
+    mbar_init(&ctl.dp_empty, 8);
     mbar_init(&ctl.drain, 1);
     fence_mbar_init();
   }
@@ -109,31 +142,61 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (CS == 2) cluster_sync();  // the partner's barriers are initialised before any load or commit reaches them
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
+  constexpr uint16_t kPair = (1u << CS) - 1u;
 
   if (warp == 0) {
+    // producer: Q (staged in the dO region), the ring's K / V units in consumption
+    // order K_0, V_0, K_1, V_1, ..., and dO once the compute warps have copied Q to TMEM
     if (lane == 0 && nt > 0) {
-      mbar_arrive_expect_tx(&ctl.a_full, C::A_BYTES);
-      for (int c = 0; c < C::QCH; ++c) tma_load_3d(sA + c * C::BM * 128, &tmA, &ctl.a_full, c * 64, it.head, it.q_row0);
+      mbar_arrive_expect_tx(&ctl.q_full, C::A_BYTES);
+      for (int c = 0; c < C::QCH; ++c) tma_load_3d(sA + c * C::BM * 128, &tmQ, &ctl.q_full, c * 64, it.head, it.q_row0);
+      bool do_loaded = false;
       int idx = 0;
-      // the ring reuses the staging memory once the compute warps have copied A into TMEM
-      bool ok = mbar_wait(&ctl.a_tmem, 0, fs);
+      bool ok = true;
       for (int j = 0; j < nt && ok; ++j) {
         int r, t;
         walk_tile(it, j, r, t);
         const int key_row = it.reg[r].row0 + t * C::BN;
-        for (int u = 0; u < C::KU && ok; ++u, ++idx) {
-          const int slot = idx % C::NST;
-          if (!(ok = mbar_wait(&ctl.ring_empty[slot], ((idx / C::NST) & 1) ^ 1, fs))) break;
-          mbar_arrive_expect_tx(&ctl.ring_full[slot], C::UNIT_BYTES);
-          uint8_t* dst = sRing + slot * C::UNIT_BYTES;
-          for (int c = 0; c < 2; ++c)
-            tma_load_3d(dst + c * C::BN * 128, &tmB, &ctl.ring_full[slot], (2 * u + c) * 64, kvh, key_row);
+        for (int kind = 0; kind < 2 && ok; ++kind) {
+          const CUtensorMap* tm = kind == 0 ? &tmK : &tmV;
+          for (int u = 0; u < C::KU && ok; ++u, ++idx) {
+            const int slot = idx % C::NST;
+            // with CS = 2 this barrier completes once both CTAs' MMAs have read the slot
+            if (!(ok = mbar_wait(&ctl.ring_empty[slot], ((idx / C::NST) & 1) ^ 1, fs))) break;
+            mbar_arrive_expect_tx(&ctl.ring_full[slot], C::UNIT_BYTES);
+            uint8_t* dst = sRing + slot * C::UNIT_BYTES;
+            if (CS == 1) {
+              for (int c = 0; c < 2; ++c)
+                tma_load_3d(dst + c * C::BN * 128, tm, &ctl.ring_full[slot], (2 * u + c) * 64, kvh, key_row);
+            } else {
+              const int c = (int)crank;  // this CTA's chunk of the unit, for both CTAs
+              tma_load_3d_mc(dst + c * C::BN * 128, tm, &ctl.ring_full[slot], (2 * u + c) * 64, kvh, key_row, kPair);
+            }
+          }
+          if (j == 0 && kind == 0 && ok) {
+            // dO replaces the staged Q once the compute warps have copied Q into TMEM
+            if (!(ok = mbar_wait(&ctl.q_tmem, 0, fs))) break;
+            mbar_arrive_expect_tx(&ctl.do_full, C::A_BYTES);
+            for (int c = 0; c < C::QCH; ++c)
+              tma_load_3d(sA + c * C::BM * 128, &tmDO, &ctl.do_full, c * 64, it.head, it.q_row0);
+            do_loaded = true;
+          }
+        }
+      }
+      if (ok && CS == 2) {
+        // the partner's last commits land on this CTA's empty barriers: wait for them
+        // before leaving
+        for (int back = 1; back <= C::NST && back <= idx && ok; ++back) {
+          const int i2 = idx - back;
+          ok = mbar_wait(&ctl.ring_empty[i2 % C::NST], (i2 / C::NST) & 1, fs);
         }
       }
       if (!ok) {
-        mbar_wait_drain(&ctl.a_full, 0, kWaitLimitNs);
+        mbar_wait_drain(&ctl.q_full, 0, kWaitLimitNs);
+        if (do_loaded) mbar_wait_drain(&ctl.do_full, 0, kWaitLimitNs);
         for (int back = 1; back <= C::NST && back <= idx; ++back) {
           const int i2 = idx - back;
           mbar_wait_drain(&ctl.ring_full[i2 % C::NST], (i2 / C::NST) & 1, kWaitLimitNs);
@@ -141,32 +204,49 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
       }
     }
   } else if (warp == 1) {
+    // S_j = Q K_j^T (A from TMEM), then dP_j = dO V_j^T (A from shared memory); each
+    // waits until the compute warps have loaded the previous block's result
     if (nt > 0) {
       constexpr uint32_t idS = idesc_bf16(128, C::BN, 0, 0);
       const uint32_t aRing = smem_u32(sRing);
-      bool ok = mbar_wait(&ctl.a_tmem, 0, fs);  // A copied into TMEM
-      tc_fence_after();
+      const uint64_t adesc = sdesc_sw128(smem_u32(sA), 16, 1024);
+      bool ok = mbar_wait(&ctl.q_tmem, 0, fs);  // Q copied into TMEM
       int idx = 0;
       for (int j = 0; j < nt && ok; ++j) {
-        const uint32_t b = j & 1;
-        if (!(ok = mbar_wait(&ctl.s_empty[b], ((j >> 1) & 1) ^ 1, fs))) break;
-        const uint32_t tS = tmem + b * C::BN;
-        for (int u = 0; u < C::KU && ok; ++u, ++idx) {
-          const int slot = idx % C::NST;
-          if (!(ok = mbar_wait(&ctl.ring_full[slot], (idx / C::NST) & 1, fs))) break;
-          tc_fence_after();
-          const uint64_t bdesc = sdesc_sw128(aRing + slot * C::UNIT_BYTES, 16, 1024);
-          if (elect_one()) {
-#pragma unroll
-            for (int c = 0; c < 2; ++c)
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                mma_bf16_ts(tS, tmem + C::TM_A + 8 * ((2 * u + c) * 4 + k), sdesc_add(bdesc, c * C::BN * 128 + k * 32),
-                            idS, (u | c | k) != 0);
-            mma_commit(&ctl.ring_empty[slot]);
-            if (u == C::KU - 1) mma_commit(&ctl.s_full[b]);
+        for (int kind = 0; kind < 2 && ok; ++kind) {
+          if (kind == 0) {
+            if (j > 0 && !(ok = mbar_wait(&ctl.s_empty, (j - 1) & 1, fs))) break;
+          } else {
+            if (j == 0 && !(ok = mbar_wait(&ctl.do_full, 0, fs))) break;
+            if (j > 0 && !(ok = mbar_wait(&ctl.dp_empty, (j - 1) & 1, fs))) break;
           }
-          __syncwarp();
+          const uint32_t tD = tmem + (kind == 0 ? C::TM_S : C::TM_DP);
+          for (int u = 0; u < C::KU && ok; ++u, ++idx) {
+            const int slot = idx % C::NST;
+            if (!(ok = mbar_wait(&ctl.ring_full[slot], (idx / C::NST) & 1, fs))) break;
+            tc_fence_after();
+            const uint64_t bdesc = sdesc_sw128(aRing + slot * C::UNIT_BYTES, 16, 1024);
+            if (elect_one()) {
+#pragma unroll
+              for (int c = 0; c < 2; ++c)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const int kc = 2 * u + c;  // 64-column chunk of the contraction
+                  if (kind == 0)
+                    mma_bf16_ts(tD, tmem + C::TM_Q + 8 * (kc * 4 + k), sdesc_add(bdesc, c * C::BN * 128 + k * 32),
+                                idS, (u | c | k) != 0);
+                  else
+                    mma_bf16_ss(tD, sdesc_add(adesc, kc * C::BM * 128 + k * 32),
+                                sdesc_add(bdesc, c * C::BN * 128 + k * 32), idS, (u | c | k) != 0);
+                }
+              if (CS == 1)
+                mma_commit(&ctl.ring_empty[slot]);
+              else
+                mma_commit_mc(&ctl.ring_empty[slot], kPair);
+              if (u == C::KU - 1) mma_commit(kind == 0 ? &ctl.s_full : &ctl.dp_full);
+            }
+            __syncwarp();
+          }
         }
       }
       if (elect_one()) mma_commit(&ctl.drain);
@@ -174,21 +254,21 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
       mbar_wait_drain(&ctl.drain, 0, kWaitLimitNs);
     }
   } else {
-    // thread <-> query row, half <-> 64 key columns; each tile yields 128 bytes of one row of the output block
+    // thread <-> query row, half <-> 64 key columns of each block
     const uint32_t wq = warp & 3, half = (warp - 2) >> 2;
     const int row = (int)(wq * 32 + lane);
     const uint32_t tl = tmem + ((wq * 32) << 16);
     const int qpos = it.q_pos0 + row;
     const bool valid = row < it.q_rows;
     const int64_t rix = (int64_t)it.head * a.T + it.q_row0 + row;
-    const float lse2 = (MODE == 0 && valid) ? a.lse2[rix] : INFINITY;
-    const float delta = (MODE == 1 && valid) ? a.delta[rix] : 0.f;
+    const float lse2 = valid ? a.lse2[rix] : INFINITY;
+    const float delta = valid ? a.delta[rix] : 0.f;
     constexpr int HC = C::BN / 2;
     bool ok = true;
     if (nt > 0) {
-      // copy this row of the resident operand into TMEM (the A operand of the
-      // GEMM): the first half's warps take 64-column chunks 0-3, the second's 4-7
-      if ((ok = mbar_wait(&ctl.a_full, 0, fs))) {
+      // copy this row of Q into TMEM (the A operand of S): the first half's warps take
+      // 64-column chunks 0-3, the second's 4-7
+      if ((ok = mbar_wait(&ctl.q_full, 0, fs))) {
 #pragma unroll
         for (int cc = 0; cc < C::QCH / 2; ++cc) {
           const int c = (int)half * (C::QCH / 2) + cc;
@@ -201,40 +281,33 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
             w[4 * u + 2] = x.z;
             w[4 * u + 3] = x.w;
           }
-          tmem_st32(tl + C::TM_A + 32 * c, w);
+          tmem_st32(tl + C::TM_Q + 32 * c, w);
         }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ctl.a_tmem);
+        if (lane == 0) mbar_arrive(&ctl.q_tmem);
       }
     }
+    const float2 sl2v = make_float2(a.scale_log2, a.scale_log2), nl = make_float2(-lse2, -lse2);
+    const float2 dl = make_float2(delta, delta);
     for (int j = 0; j < nt && ok; ++j) {
-      const uint32_t b = j & 1;
       const size_t boff = (size_t)(blk0 + j) * (kBlkBytes / 2) + (size_t)row * C::BN + HC * half;
-      // dS needs this block's P: its loads are issued before waiting for S
-      uint4 pin[HC / 8];
-      if (MODE == 1) {
-        const uint4* src = reinterpret_cast<const uint4*>(a.p_blocks + boff);
+      float p[HC];
+      {
+        if (!(ok = mbar_wait(&ctl.s_full, j & 1, fs))) break;
+        tc_fence_after();
 #pragma unroll
-        for (int v = 0; v < HC / 8; ++v) pin[v] = src[v];
-      }
-      if (!(ok = mbar_wait(&ctl.s_full[b], (j >> 1) & 1, fs))) break;
-      tc_fence_after();
-      float s[HC];
+        for (int c4 = 0; c4 < HC / 32; ++c4) {
+          uint32_t rr[32];
+          tmem_ld32(tl + C::TM_S + HC * half + c4 * 32, rr);
 #pragma unroll
-      for (int c4 = 0; c4 < HC / 32; ++c4) {
-        uint32_t rr[32];
-        tmem_ld32(tl + b * C::BN + HC * half + c4 * 32, rr);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c4 * 32 + i] = __uint_as_float(rr[i]);
-      }
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl.s_empty[b]);
-      uint4* dst = reinterpret_cast<uint4*>(a.out_blocks + boff);
-      if (MODE == 0) {
+          for (int i = 0; i < 32; ++i) p[c4 * 32 + i] = __uint_as_float(rr[i]);
+        }
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl.s_empty);
         int r, t;
         walk_tile(it, j, r, t);
         const KeyRegion& kr = it.reg[r];
@@ -243,41 +316,65 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
         if (a.window > 0) lo = max(0, qpos - a.window + 1 - kr.pos0);
         const int hi = min(kr.count - 1, qpos - kr.pos0);
         const int clo = lo - kl0, chi = hi - kl0;
-        const float2 sl2v = make_float2(a.scale_log2, a.scale_log2), nl = make_float2(-lse2, -lse2);
+        // each thread writes its row's 128 bytes as four whole 32-byte sectors
+        __nv_bfloat16* dst = a.p_out + boff;
 #pragma unroll
-        for (int v = 0; v < HC / 8; ++v) {
-          uint32_t w[4];
+        for (int v = 0; v < HC / 16; ++v) {
+          uint32_t w[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 8 * v + 2 * e;
-            const float2 x = ffma2(make_float2(s[c], s[c + 1]), sl2v, nl);
+          for (int e = 0; e < 8; ++e) {
+            const int c = 16 * v + 2 * e;
+            const float2 x = ffma2(make_float2(p[c], p[c + 1]), sl2v, nl);
             float p0 = ex2_approx(x.x);
             float p1 = ex2_approx(x.y);
             p0 = (c < clo || c > chi) ? 0.f : p0;
             p1 = (c + 1 < clo || c + 1 > chi) ? 0.f : p1;
+            p[c] = p0;
+            p[c + 1] = p1;
             w[e] = pack_bf16x2(p0, p1);
           }
-          dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+          st_global_v8(dst + 16 * v, w);
         }
-      } else {
-        const float2 dl = make_float2(delta, delta);
+      }
+      if (!(ok = mbar_wait(&ctl.dp_full, j & 1, fs))) break;
+      tc_fence_after();
+      float dpv[HC];
 #pragma unroll
-        for (int v = 0; v < HC / 8; ++v) {
-          const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&pin[v]);
-          uint32_t w[4];
+      for (int c4 = 0; c4 < HC / 32; ++c4) {
+        uint32_t rr[32];
+        tmem_ld32(tl + C::TM_DP + HC * half + c4 * 32, rr);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 8 * v + 2 * e;
-            const float2 ds = fmul2(__bfloat1622float2(p2[e]), fsub2(make_float2(s[c], s[c + 1]), dl));
-            w[e] = pack_bf16x2(ds.x, ds.y);
-          }
-          dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int i = 0; i < 32; ++i) dpv[c4 * 32 + i] = __uint_as_float(rr[i]);
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl.dp_empty);
+      __nv_bfloat16* dst = a.ds_out + boff;
+#pragma unroll
+      for (int v = 0; v < HC / 16; ++v) {
+        uint32_t w[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int c = 16 * v + 2 * e;
+          const float2 ds = fmul2(make_float2(p[c], p[c + 1]), fsub2(make_float2(dpv[c], dpv[c + 1]), dl));
+          w[e] = pack_bf16x2(ds.x, ds.y);
         }
+        st_global_v8(dst + 16 * v, w);
       }
     }
   }
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
+  if (CS == 2) {
+    // once both CTAs are here neither issues another load or commit; a CTA whose
+    // waits gave up may still have the partner's earlier ones in flight towards it,
+    // so it stays resident a while before releasing its memory
+    cluster_sync();
+    if (threadIdx.x == 0 && ctl.abort_flag) sleep_for_ns(200000);
+    __syncthreads();
+  }
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
 }
@@ -594,20 +691,36 @@ cudaError_t set_smem(K kernel, int bytes, bool& done) {
 
 }  // namespace
 
-cudaError_t launch_pds(int mode, const CUtensorMap& tA, const CUtensorMap& tB, const PdsArgs& a, int n_items,
-                       cudaStream_t st) {
+cudaError_t launch_pds_fused(const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
+                             const CUtensorMap& tv, const PdsArgs& a, int n_items, bool pair_heads, cudaStream_t st) {
   if (n_items <= 0) return cudaSuccess;
-  static bool s0 = false, s1 = false;
+  static bool s1 = false, s2 = false;
   cudaError_t e;
-  if (mode == 0) {
-    if ((e = set_smem(pds_kernel<0>, PdsCfg::SMEM_BYTES, s0)) != cudaSuccess) return e;
-    pds_kernel<0><<<n_items, kPdsThreads, PdsCfg::SMEM_BYTES, st>>>(tA, tB, a);
-  } else {
-    if ((e = set_smem(pds_kernel<1>, PdsCfg::SMEM_BYTES, s1)) != cudaSuccess) return e;
-    pds_kernel<1><<<n_items, kPdsThreads, PdsCfg::SMEM_BYTES, st>>>(tA, tB, a);
+  // pairs of q-heads of one kv-head group share the walk: items 2i and 2i + 1 of the
+  // list are the same query rows for two heads of a group whenever the group size is even
+  if (pair_heads) {
+    if ((e = set_smem(pds_fused_kernel<2>, PdsFCfg::SMEM_BYTES, s2)) != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)n_items);
+    cfg.blockDim = dim3(kPdsThreads);
+    cfg.dynamicSmemBytes = PdsFCfg::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, pds_fused_kernel<2>, tq, tdo, tk, tv, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
   }
+  if ((e = set_smem(pds_fused_kernel<1>, PdsFCfg::SMEM_BYTES, s1)) != cudaSuccess) return e;
+  pds_fused_kernel<1><<<n_items, kPdsThreads, PdsFCfg::SMEM_BYTES, st>>>(tq, tdo, tk, tv, a);
   return cudaGetLastError();
 }
+
 
 cudaError_t launch_xtg(const CUtensorMap& tBlk, const CUtensorMap& tB, const XtgArgs& a, int n_items, cudaStream_t st) {
   if (n_items <= 0) return cudaSuccess;

@@ -105,15 +105,19 @@ struct PdsArgs {
   const int32_t* block_base;
   const float* lse2;
   const float* delta;
-  const __nv_bfloat16* p_blocks;  // mode 1 input
-  __nv_bfloat16* out_blocks;      // mode 0: P blocks, mode 1: dS blocks
+  __nv_bfloat16* p_out;   // P blocks (written)
+  __nv_bfloat16* ds_out;  // dS blocks (written)
   int T, Hq, Hkv, window;
   float scale_log2;
   uint32_t* status;
-  int64_t n_blocks = 0;  // P / dS blocks in p_blocks and out_blocks
+  int64_t n_blocks = 0;  // blocks in p_out and ds_out
 };
-cudaError_t launch_pds(int mode, const CUtensorMap& tA, const CUtensorMap& tB, const PdsArgs& a, int n_items,
-                       cudaStream_t st);
+// Both blocks of every (query tile, key tile) pair in one pass: P = exp(S - LSE)
+// into a.p_out and dS = P (dP - Delta) into a.ds_out.  pair_heads: items 2i and
+// 2i + 1 are the same query rows for two q-heads of one kv-head group (n_items even);
+// each pair runs as a 2-CTA cluster that shares its K / V loads.
+cudaError_t launch_pds_fused(const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
+                             const CUtensorMap& tv, const PdsArgs& a, int n_items, bool pair_heads, cudaStream_t st);
 
 struct XtgArgs {
   const XTItem* items;

@@ -64,6 +64,8 @@ SMALL = [
     # (38 query tiles x 8 heads x 2 halves), so the dK/dV GEMMs split the prompt
     # tiles and the fixed-order reduction runs
     ("d512-split-prompt-tiles", 200, [100] * 36, 8, 1, 512, 0),
+    # an odd group size: the P / dS pass cannot pair q-heads and runs one CTA per tile
+    ("d512-group3-window", 260, [150, 0, 90], 3, 1, 512, 64),
 ]
 
 
