@@ -396,13 +396,16 @@ WsLayout ws_layout(int64_t T, int Hq, int D, int nslots, int64_t n_blocks) {
 }
 
 // [n_blocks, 128, 128] bf16 blocks, box 64 columns x box_rows rows x 1 block, 128-byte swizzle.
+// A P / dS block is 16 column groups x 128 rows x 8 keys; seen here as
+// [block][group][row quarter][32 rows x 8 keys].  box_rows = 64: 64 rows, all 16
+// groups (a transposed-GEMM stage); box_rows = 128: all rows, 8 groups (a dQ stage).
 int make_block_tmap(CUtensorMap* m, const void* base, int64_t n_blocks, int box_rows) {
-  cuuint64_t dims[3] = {128, 128, (cuuint64_t)n_blocks};
-  cuuint64_t strides[2] = {256, 128 * 256};
-  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  cuuint64_t dims[4] = {256, 4, 16, (cuuint64_t)n_blocks};
+  cuuint64_t strides[3] = {512, 2048, 32768};
+  cuuint32_t box[4] = {256, (cuuint32_t)(box_rows / 32), box_rows == 64 ? 16u : 8u, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? DUALKV_OK : DUALKV_ERR_CUDA;
 }

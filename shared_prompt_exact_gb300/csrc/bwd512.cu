@@ -24,6 +24,11 @@ namespace {
 
 constexpr int kD = 512;
 constexpr int kBlkBytes = 128 * 128 * 2;  // one P or dS block
+// Inside a block, element (query row r, key column c) sits at
+//   (c / 8) * 1024 + r * 8 + c % 8     (bf16 elements)
+// -- 16 column groups of 8 keys, each 128 rows x 16 bytes.  A warp's 32 rows of one
+// group are 512 contiguous bytes, so the P / dS stores are whole cache lines, and the
+// GEMMs read the blocks as unswizzled core matrices (8 rows x 16 bytes).
 
 __device__ __forceinline__ void walk_tile(const QTileItem& it, int j, int& r, int& t) {
   const int n0 = it.reg[0].t_hi - it.reg[0].t_lo;
@@ -292,7 +297,8 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
     const float2 sl2v = make_float2(a.scale_log2, a.scale_log2), nl = make_float2(-lse2, -lse2);
     const float2 dl = make_float2(delta, delta);
     for (int j = 0; j < nt && ok; ++j) {
-      const size_t boff = (size_t)(blk0 + j) * (kBlkBytes / 2) + (size_t)row * C::BN + HC * half;
+      // this thread's 8 column groups of the block, 8 keys (16 bytes) each
+      const size_t boff = (size_t)(blk0 + j) * (kBlkBytes / 2) + (size_t)(8 * half) * 1024 + (size_t)row * 8;
       float p[HC];
       {
         if (!(ok = mbar_wait(&ctl.s_full, j & 1, fs))) break;
@@ -316,14 +322,13 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
         if (a.window > 0) lo = max(0, qpos - a.window + 1 - kr.pos0);
         const int hi = min(kr.count - 1, qpos - kr.pos0);
         const int clo = lo - kl0, chi = hi - kl0;
-        // each thread writes its row's 128 bytes as four whole 32-byte sectors
-        __nv_bfloat16* dst = a.p_out + boff;
+        uint4* dst = reinterpret_cast<uint4*>(a.p_out + boff);
 #pragma unroll
-        for (int v = 0; v < HC / 16; ++v) {
-          uint32_t w[8];
+        for (int v = 0; v < HC / 8; ++v) {
+          uint32_t w[4];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int c = 16 * v + 2 * e;
+          for (int e = 0; e < 4; ++e) {
+            const int c = 8 * v + 2 * e;
             const float2 x = ffma2(make_float2(p[c], p[c + 1]), sl2v, nl);
             float p0 = ex2_approx(x.x);
             float p1 = ex2_approx(x.y);
@@ -333,7 +338,7 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
             p[c + 1] = p1;
             w[e] = pack_bf16x2(p0, p1);
           }
-          st_global_v8(dst + 16 * v, w);
+          dst[v * 128] = make_uint4(w[0], w[1], w[2], w[3]);  // column group 8 * half + v (2048 bytes apart)
         }
       }
       if (!(ok = mbar_wait(&ctl.dp_full, j & 1, fs))) break;
@@ -350,17 +355,17 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl.dp_empty);
-      __nv_bfloat16* dst = a.ds_out + boff;
+      uint4* dst = reinterpret_cast<uint4*>(a.ds_out + boff);
 #pragma unroll
-      for (int v = 0; v < HC / 16; ++v) {
-        uint32_t w[8];
+      for (int v = 0; v < HC / 8; ++v) {
+        uint32_t w[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int c = 16 * v + 2 * e;
+        for (int e = 0; e < 4; ++e) {
+          const int c = 8 * v + 2 * e;
           const float2 ds = fmul2(make_float2(p[c], p[c + 1]), fsub2(make_float2(dpv[c], dpv[c + 1]), dl));
           w[e] = pack_bf16x2(ds.x, ds.y);
         }
-        st_global_v8(dst + 16 * v, w);
+        dst[v * 128] = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
   }
@@ -453,8 +458,8 @@ __global__ void __launch_bounds__(192, 1)
         if (!(ok = mbar_wait(&ctl.empty[slot], ((i / C::NST) & 1) ^ 1, fs))) break;
         mbar_arrive_expect_tx(&ctl.full[slot], C::STAGE_BYTES);
         uint8_t* st = smem + slot * C::STAGE_BYTES;
-        for (int kc = 0; kc < 2; ++kc)
-          tma_load_3d(st + kc * 64 * 128, &tmBlk, &ctl.full[slot], kc * 64, e.sub * 64, e.block);
+        // rows [64 sub, 64 sub + 64) of the block, all 16 column groups: [group][row][8 keys]
+        tma_load_4d(st, &tmBlk, &ctl.full[slot], 0, 2 * e.sub, 0, e.block);
         for (int c = 0; c < 8; ++c)
           tma_load_3d(st + C::A_BYTES + c * 64 * 128, &tmB, &ctl.full[slot], c * 64, e.head, e.q_row0);
       }
@@ -474,7 +479,8 @@ __global__ void __launch_bounds__(192, 1)
         const int slot = i % C::NST;
         if (!(ok = mbar_wait(&ctl.full[slot], (i / C::NST) & 1, fs))) break;
         tc_fence_after();
-        const uint64_t ad = sdesc_sw128(base + slot * C::STAGE_BYTES, 64 * 128, 1024);
+        // A = block^T, MN-major (keys): 8-key groups 1024 bytes apart, 8-row groups 128
+        const uint64_t ad = sdesc_noswz(base + slot * C::STAGE_BYTES, 128, 1024);
         const uint64_t bd = sdesc_sw128(base + slot * C::STAGE_BYTES + C::A_BYTES, 64 * 128, 1024);
         const uint32_t acc0 = i > 0 ? 1u : 0u;
         if (elect_one()) {
@@ -482,7 +488,7 @@ __global__ void __launch_bounds__(192, 1)
           for (int k = 0; k < 4; ++k)
 #pragma unroll
             for (int nh = 0; nh < 2; ++nh)
-              mma_bf16_ss(tmem + nh * 256, sdesc_add(ad, k * 16 * 128), sdesc_add(bd, nh * 4 * 64 * 128 + k * 16 * 128),
+              mma_bf16_ss(tmem + nh * 256, sdesc_add(ad, k * 16 * 16), sdesc_add(bd, nh * 4 * 64 * 128 + k * 16 * 128),
                           idX, k > 0 ? 1u : acc0);
           mma_commit(&ctl.empty[slot]);
         }
@@ -609,7 +615,8 @@ __global__ void __launch_bounds__(192, 1)
         if (!(ok = mbar_wait(&ctl.empty[slot], ((i / C::NST) & 1) ^ 1, fs))) break;
         mbar_arrive_expect_tx(&ctl.full[slot], C::STAGE_BYTES);
         uint8_t* st = smem + slot * C::STAGE_BYTES;
-        tma_load_3d(st, &tmBlk, &ctl.full[slot], half * 64, 0, blk0 + j);
+        // keys [64 half, 64 half + 64) of the block: column groups 8 half .. 8 half + 7, all rows
+        tma_load_4d(st, &tmBlk, &ctl.full[slot], 0, 0, 8 * half, blk0 + j);
         for (int c = 0; c < 8; ++c) tma_load_3d(st + C::A_BYTES + c * 64 * 128, &tmK, &ctl.full[slot], c * 64, kvh, key_row);
       }
       if (!ok) {
@@ -628,7 +635,8 @@ __global__ void __launch_bounds__(192, 1)
         const int slot = i % C::NST;
         if (!(ok = mbar_wait(&ctl.full[slot], (i / C::NST) & 1, fs))) break;
         tc_fence_after();
-        const uint64_t ad = sdesc_sw128(base + slot * C::STAGE_BYTES, 16, 1024);
+        // A = dS, K-major (keys): 8-key groups 2048 bytes apart, 8-row groups 128
+        const uint64_t ad = sdesc_noswz(base + slot * C::STAGE_BYTES, 2048, 128);
         const uint64_t bd = sdesc_sw128(base + slot * C::STAGE_BYTES + C::A_BYTES, 64 * 128, 1024);
         const uint32_t acc0 = i > 0 ? 1u : 0u;
         if (elect_one()) {
@@ -636,7 +644,7 @@ __global__ void __launch_bounds__(192, 1)
           for (int k = 0; k < 4; ++k)
 #pragma unroll
             for (int nh = 0; nh < 2; ++nh)
-              mma_bf16_ss(tmem + nh * 256, sdesc_add(ad, k * 32), sdesc_add(bd, nh * 4 * 64 * 128 + k * 16 * 128), idQ,
+              mma_bf16_ss(tmem + nh * 256, sdesc_add(ad, k * 2 * 2048), sdesc_add(bd, nh * 4 * 64 * 128 + k * 16 * 128), idQ,
                           k > 0 ? 1u : acc0);
           mma_commit(&ctl.empty[slot]);
         }

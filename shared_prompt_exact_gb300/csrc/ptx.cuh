@@ -145,6 +145,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// 4-D tiled load; c0 (innermost) must be a multiple of 8 bf16 elements.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
+                                            int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+      "[%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
 // The same load delivered to every CTA of the cluster named in `mask`, at the same
 // shared-memory offset in each; the bytes complete on each destination's barrier at
 // the offset of `bar`.
@@ -188,6 +197,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= 1ull << 46;
   d |= 2ull << 61;
+  return d;
+}
+
+// Shared-memory matrix descriptor without swizzle: the operand is a grid of core
+// matrices of 8 rows x 16 bytes, each 128 contiguous bytes.  K-major: lbo = byte
+// distance between core matrices adjacent along K, sbo = along M/N.  MN-major: lbo
+// along K, sbo along M/N (16-byte groups of M/N elements).
+__device__ __forceinline__ uint64_t sdesc_noswz(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
   return d;
 }
 
@@ -326,13 +348,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a
 // 128-byte-swizzled tile whose rows are 128 bytes (the layout TMA writes with
 // CU_TENSOR_MAP_SWIZZLE_128B and tcgen05 reads with swizzle mode 2).
-// One 32-byte global store (address 32-byte aligned): a whole L2 sector per thread,
-// where two 16-byte stores would each send a half-filled sector.
-__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
-  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-               "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-               : "memory");
-}
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
   return row * 128u + ((chunk ^ (row & 7u)) << 4);
 }
