@@ -557,8 +557,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* out, const
     Dq512Args qa{pl->dq_items, pl->block_base, static_cast<__nv_bfloat16*>(dq), (int)T, Hq, Hkv, scale, status,
                  pl->n_blocks};
     if (timed(DUALKV_KERNEL_DKV, st, [&] {
-          const bool pair_heads = (Hq / Hkv) % 2 == 0 && pl->n_dq % 2 == 0;
-          cudaError_t e = launch_pds_fused(tq, tdo, tk, tv, pa5, pl->n_dq, pair_heads, st);
+          cudaError_t e = launch_pds_fused(tq, tdo, tk, tv, pa5, pl->n_dq, st);
           if (e == cudaSuccess) e = launch_xtg(tP64, tdo64, xv, pl->n_xt, st);
           if (e == cudaSuccess) e = launch_xtg(tDS64, tq64, xk, pl->n_xt, st);
           return e;

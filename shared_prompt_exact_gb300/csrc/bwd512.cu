@@ -53,12 +53,6 @@ constexpr int kPdsThreads = 320;
 // 128 KB), and K / V tiles stream through a 3-unit ring; S and dP have one TMEM
 // buffer each (128 columns): each block's two GEMMs keep the pipe busy while the
 // compute warps drain the other one.
-//
-// CS = 2: the two CTAs of a cluster take the same query rows for two q-heads of
-// one kv-head group, so they walk the same K / V tiles.  Each unit of the ring
-// then arrives by one multicast load per CTA (one 64-column chunk each, delivered
-// to both), which halves the L2 -> SM traffic of the walk; a slot is refilled once
-// the MMAs of both CTAs have read it (each commits to both CTAs' empty barrier).
 struct PdsFCfg {
   static constexpr int BM = 128, BN = 128;
   static constexpr int QCH = kD / 64;              // 64-column chunks of Q / dO / K / V
@@ -80,21 +74,10 @@ struct PdsFCtl {
   int abort_flag;
 };
 
-__device__ __forceinline__ bool same_walk(const QTileItem& x, const QTileItem& y) {
-  bool eq = x.q_row0 == y.q_row0 && x.q_pos0 == y.q_pos0 && x.q_rows == y.q_rows;
-#pragma unroll
-  for (int r = 0; r < 2; ++r)
-    eq = eq && x.reg[r].row0 == y.reg[r].row0 && x.reg[r].pos0 == y.reg[r].pos0 && x.reg[r].count == y.reg[r].count &&
-         x.reg[r].t_lo == y.reg[r].t_lo && x.reg[r].t_hi == y.reg[r].t_hi;
-  return eq;
-}
-
-template <int CS>
 __global__ void __launch_bounds__(kPdsThreads, 1)
     pds_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const PdsArgs a) {
-  static_assert(CS == 1 || CS == 2, "one CTA, or a pair sharing the K / V walk");
   using C = PdsFCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -106,20 +89,8 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
   const int blk0 = a.block_base[blockIdx.x];
   const int nt_all = (it.reg[0].t_hi - it.reg[0].t_lo) + (it.reg[1].t_hi - it.reg[1].t_lo);
   // an item outside the tensors or naming blocks past the block array does nothing
-  bool item_ok = qtile_ok(it, a.T, a.Hq, C::BM, C::BN) && blk0 >= 0 && (int64_t)blk0 + nt_all <= a.n_blocks;
-  const int gsz = a.Hq / a.Hkv;
-  const int kvh = it.head / gsz;
-  uint32_t crank = 0;
-  if (CS == 2) {
-    // both CTAs of the pair take the same decision: both items valid and walking the
-    // same key tiles of one kv-head
-    crank = cluster_ctarank();
-    const QTileItem pit = a.items[blockIdx.x ^ 1u];
-    const int pblk0 = a.block_base[blockIdx.x ^ 1u];
-    const int pnt = (pit.reg[0].t_hi - pit.reg[0].t_lo) + (pit.reg[1].t_hi - pit.reg[1].t_lo);
-    const bool pok = qtile_ok(pit, a.T, a.Hq, C::BM, C::BN) && pblk0 >= 0 && (int64_t)pblk0 + pnt <= a.n_blocks;
-    item_ok = item_ok && pok && same_walk(it, pit) && pit.head / gsz == kvh;
-  }
+  const bool item_ok = qtile_ok(it, a.T, a.Hq, C::BM, C::BN) && blk0 >= 0 && (int64_t)blk0 + nt_all <= a.n_blocks;
+  const int kvh = it.head / (a.Hq / a.Hkv);
   const int nt = item_ok ? nt_all : 0;
   const uint32_t warp = warp_id(), lane = lane_id();
   FailState fs{&ctl.abort_flag, a.status};
@@ -132,7 +103,7 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
     mbar_init(&ctl.do_full, 1);
     for (int i = 0; i < C::NST; ++i) {
       mbar_init(&ctl.ring_full[i], 1);
-      mbar_init(&ctl.ring_empty[i], CS);
+      mbar_init(&ctl.ring_empty[i], 1);
     }
     mbar_init(&ctl.s_full, 1);
     mbar_init(&ctl.s_empty, 8);
@@ -147,10 +118,8 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (CS == 2) cluster_sync();  // the partner's barriers are initialised before any load or commit reaches them
   tc_fence_after();
   const uint32_t tmem = ctl.tmem_base;
-  constexpr uint16_t kPair = (1u << CS) - 1u;
 
   if (warp == 0) {
     // producer: Q (staged in the dO region), the ring's K / V units in consumption
@@ -169,17 +138,11 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
           const CUtensorMap* tm = kind == 0 ? &tmK : &tmV;
           for (int u = 0; u < C::KU && ok; ++u, ++idx) {
             const int slot = idx % C::NST;
-            // with CS = 2 this barrier completes once both CTAs' MMAs have read the slot
             if (!(ok = mbar_wait(&ctl.ring_empty[slot], ((idx / C::NST) & 1) ^ 1, fs))) break;
             mbar_arrive_expect_tx(&ctl.ring_full[slot], C::UNIT_BYTES);
             uint8_t* dst = sRing + slot * C::UNIT_BYTES;
-            if (CS == 1) {
-              for (int c = 0; c < 2; ++c)
-                tma_load_3d(dst + c * C::BN * 128, tm, &ctl.ring_full[slot], (2 * u + c) * 64, kvh, key_row);
-            } else {
-              const int c = (int)crank;  // this CTA's chunk of the unit, for both CTAs
-              tma_load_3d_mc(dst + c * C::BN * 128, tm, &ctl.ring_full[slot], (2 * u + c) * 64, kvh, key_row, kPair);
-            }
+            for (int c = 0; c < 2; ++c)
+              tma_load_3d(dst + c * C::BN * 128, tm, &ctl.ring_full[slot], (2 * u + c) * 64, kvh, key_row);
           }
           if (j == 0 && kind == 0 && ok) {
             // dO replaces the staged Q once the compute warps have copied Q into TMEM
@@ -189,14 +152,6 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
               tma_load_3d(sA + c * C::BM * 128, &tmDO, &ctl.do_full, c * 64, it.head, it.q_row0);
             do_loaded = true;
           }
-        }
-      }
-      if (ok && CS == 2) {
-        // the partner's last commits land on this CTA's empty barriers: wait for them
-        // before leaving
-        for (int back = 1; back <= C::NST && back <= idx && ok; ++back) {
-          const int i2 = idx - back;
-          ok = mbar_wait(&ctl.ring_empty[i2 % C::NST], (i2 / C::NST) & 1, fs);
         }
       }
       if (!ok) {
@@ -244,10 +199,7 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
                     mma_bf16_ss(tD, sdesc_add(adesc, kc * C::BM * 128 + k * 32),
                                 sdesc_add(bdesc, c * C::BN * 128 + k * 32), idS, (u | c | k) != 0);
                 }
-              if (CS == 1)
-                mma_commit(&ctl.ring_empty[slot]);
-              else
-                mma_commit_mc(&ctl.ring_empty[slot], kPair);
+              mma_commit(&ctl.ring_empty[slot]);
               if (u == C::KU - 1) mma_commit(kind == 0 ? &ctl.s_full : &ctl.dp_full);
             }
             __syncwarp();
@@ -369,17 +321,8 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
       }
     }
   }
-  __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (CS == 2) {
-    // once both CTAs are here neither issues another load or commit; a CTA whose
-    // waits gave up may still have the partner's earlier ones in flight towards it,
-    // so it stays resident a while before releasing its memory
-    cluster_sync();
-    if (threadIdx.x == 0 && ctl.abort_flag) sleep_for_ns(200000);
-    __syncthreads();
-  }
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, C::TM_COLS);
 }
@@ -700,32 +643,12 @@ cudaError_t set_smem(K kernel, int bytes, bool& done) {
 }  // namespace
 
 cudaError_t launch_pds_fused(const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
-                             const CUtensorMap& tv, const PdsArgs& a, int n_items, bool pair_heads, cudaStream_t st) {
+                             const CUtensorMap& tv, const PdsArgs& a, int n_items, cudaStream_t st) {
   if (n_items <= 0) return cudaSuccess;
-  static bool s1 = false, s2 = false;
+  static bool s = false;
   cudaError_t e;
-  // pairs of q-heads of one kv-head group share the walk: items 2i and 2i + 1 of the
-  // list are the same query rows for two heads of a group whenever the group size is even
-  if (pair_heads) {
-    if ((e = set_smem(pds_fused_kernel<2>, PdsFCfg::SMEM_BYTES, s2)) != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)n_items);
-    cfg.blockDim = dim3(kPdsThreads);
-    cfg.dynamicSmemBytes = PdsFCfg::SMEM_BYTES;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, pds_fused_kernel<2>, tq, tdo, tk, tv, a);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
-  }
-  if ((e = set_smem(pds_fused_kernel<1>, PdsFCfg::SMEM_BYTES, s1)) != cudaSuccess) return e;
-  pds_fused_kernel<1><<<n_items, kPdsThreads, PdsFCfg::SMEM_BYTES, st>>>(tq, tdo, tk, tv, a);
+  if ((e = set_smem(pds_fused_kernel, PdsFCfg::SMEM_BYTES, s)) != cudaSuccess) return e;
+  pds_fused_kernel<<<n_items, kPdsThreads, PdsFCfg::SMEM_BYTES, st>>>(tq, tdo, tk, tv, a);
   return cudaGetLastError();
 }
 

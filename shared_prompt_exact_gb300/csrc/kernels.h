@@ -113,11 +113,9 @@ struct PdsArgs {
   int64_t n_blocks = 0;  // blocks in p_out and ds_out
 };
 // Both blocks of every (query tile, key tile) pair in one pass: P = exp(S - LSE)
-// into a.p_out and dS = P (dP - Delta) into a.ds_out.  pair_heads: items 2i and
-// 2i + 1 are the same query rows for two q-heads of one kv-head group (n_items even);
-// each pair runs as a 2-CTA cluster that shares its K / V loads.
+// into a.p_out and dS = P (dP - Delta) into a.ds_out.
 cudaError_t launch_pds_fused(const CUtensorMap& tq, const CUtensorMap& tdo, const CUtensorMap& tk,
-                             const CUtensorMap& tv, const PdsArgs& a, int n_items, bool pair_heads, cudaStream_t st);
+                             const CUtensorMap& tv, const PdsArgs& a, int n_items, cudaStream_t st);
 
 struct XtgArgs {
   const XTItem* items;
