@@ -304,7 +304,9 @@ int dualkv_selftest_timeout(uint64_t limit_ns, void* stream);
  *              the last row; the kernel's range check skips it;
  *   which = 3  the backward preprocess and dQ kernel given a dQ work list whose
  *              first entry lies past the last row; the preprocess, which checks
- *              that list before the dQ kernel reads it, empties the entry.
+ *              that list before the dQ kernel reads it, empties the entry;
+ *   which = 4  the head-dimension-512 P / dS pass (same layout with D = 512);
+ *              the first K/V tile of every CTA is never loaded.
  * The failure is recorded in the status word; a kernel whose wait ran out
  * drains its copies and tensor-core operations, frees its tensor memory and
  * returns;

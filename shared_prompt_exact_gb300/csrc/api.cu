@@ -809,8 +809,50 @@ int dualkv_plan_cache_info(int* n_plans, int64_t* device_bytes) {
   return DUALKV_OK;
 }
 
+// The head-dimension-512 P / dS pass on a tiny layout (zero inputs, P = 128, two
+// responses of 128, one head) whose first K/V ring unit is never loaded.
+static int selftest_pds512(uint64_t limit_ns, cudaStream_t st, uint32_t* status) {
+  constexpr int P = 128, N = 2, Hq = 1, Hkv = 1, D = 512;
+  const int32_t off[N + 1] = {0, 128, 256};
+  constexpr int64_t T = P + 256;
+  DevPlan* pl = nullptr;
+  int rc = get_plan(P, N, off, Hq, Hkv, D, 0, 0, Hkv, true, st, &pl);
+  if (rc) return rc;
+  const size_t tensor_bytes = (size_t)T * Hq * D * 2;
+  const WsLayout ws = ws_layout(T, Hq, D, pl->nslots, pl->n_blocks);
+  const size_t o_lse = 5 * tensor_bytes, o_ws = align256(o_lse + sizeof(float) * Hq * T),
+               total = o_ws + align256(ws.total);
+  uint8_t* mem = nullptr;
+  if (cudaMalloc(&mem, total) != cudaSuccess) return DUALKV_ERR_CUDA;
+  auto done = [&](int code) {
+    cudaStreamSynchronize(st);
+    cudaFree(mem);
+    return code;
+  };
+  if (cudaMemsetAsync(mem, 0, total, st) != cudaSuccess) return done(DUALKV_ERR_CUDA);
+  void *q = mem, *k = mem + tensor_bytes, *v = mem + 2 * tensor_bytes, *out = mem + 3 * tensor_bytes,
+       *dout = mem + 4 * tensor_bytes;
+  float* lse = reinterpret_cast<float*>(mem + o_lse);
+  uint8_t* wsb = mem + o_ws;
+  float* delta = reinterpret_cast<float*>(wsb + ws.delta);
+  float* lse2 = reinterpret_cast<float*>(wsb + ws.lse2);
+  PrepArgs pa{static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), lse, delta, lse2, T, Hq, D};
+  if (launch_prep(pa, st) != cudaSuccess) return done(DUALKV_ERR_CUDA);
+  CUtensorMap tq, tk, tv, tdo;
+  if (make_tmap(&tq, q, T, Hq, D, 128) || make_tmap(&tk, k, T, Hkv, D, 128) || make_tmap(&tv, v, T, Hkv, D, 128) ||
+      make_tmap(&tdo, dout, T, Hq, D, 128))
+    return done(DUALKV_ERR_CUDA);
+  PdsArgs a{pl->dq_items, pl->block_base, lse2, delta,
+            reinterpret_cast<__nv_bfloat16*>(wsb + ws.pblk), reinterpret_cast<__nv_bfloat16*>(wsb + ws.dsblk),
+            (int)T, Hq, Hkv, 0, 0.04419417382415922f * 1.4426950408889634f, status, pl->n_blocks};
+  a.wait_limit_ns = limit_ns;
+  a.test_skip_unit = 0;
+  if (launch_pds_fused(tq, tdo, tk, tv, a, pl->n_dq, st) != cudaSuccess) return done(DUALKV_ERR_CUDA);
+  return done(mark_use(&pl->last_use, st));
+}
+
 int dualkv_selftest_kernel(int which, uint64_t limit_ns, void* stream) {
-  if (which < 0 || which > 3) return DUALKV_ERR_INVALID;
+  if (which < 0 || which > 4) return DUALKV_ERR_INVALID;
   if (limit_ns < 1000000ull || limit_ns > 10000000000ull) return DUALKV_ERR_INVALID;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   std::lock_guard<std::mutex> lock(g_mu);
@@ -820,6 +862,7 @@ int dualkv_selftest_kernel(int which, uint64_t limit_ns, void* stream) {
   if (cudaGetDevice(&dev) != cudaSuccess) return DUALKV_ERR_CUDA;
   uint32_t* status = nullptr;
   if ((rc = status_word(dev, &status))) return rc;
+  if (which == 4) return selftest_pds512(limit_ns, st, status);
   // a tiny layout with zero inputs: P = 128 and two responses of 128, one head, D = 128
   constexpr int P = 128, N = 2, Hq = 1, Hkv = 1, D = 128;
   const int32_t off[N + 1] = {0, 128, 256};

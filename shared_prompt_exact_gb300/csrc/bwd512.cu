@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
   const int kvh = it.head / (a.Hq / a.Hkv);
   const int nt = item_ok ? nt_all : 0;
   const uint32_t warp = warp_id(), lane = lane_id();
-  FailState fs{&ctl.abort_flag, a.status};
+  FailState fs{&ctl.abort_flag, a.status, a.wait_limit_ns};
 
   if (threadIdx.x == 0) {
     if (!item_ok && a.status) atomicOr(a.status, kDevErrBounds);
@@ -139,6 +139,7 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
           for (int u = 0; u < C::KU && ok; ++u, ++idx) {
             const int slot = idx % C::NST;
             if (!(ok = mbar_wait(&ctl.ring_empty[slot], ((idx / C::NST) & 1) ^ 1, fs))) break;
+            if (idx == a.test_skip_unit) continue;  // failure-path self-test: never loaded
             mbar_arrive_expect_tx(&ctl.ring_full[slot], C::UNIT_BYTES);
             uint8_t* dst = sRing + slot * C::UNIT_BYTES;
             for (int c = 0; c < 2; ++c)
@@ -159,6 +160,7 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
         if (do_loaded) mbar_wait_drain(&ctl.do_full, 0, kWaitLimitNs);
         for (int back = 1; back <= C::NST && back <= idx; ++back) {
           const int i2 = idx - back;
+          if (i2 == a.test_skip_unit) continue;  // never loaded
           mbar_wait_drain(&ctl.ring_full[i2 % C::NST], (i2 / C::NST) & 1, kWaitLimitNs);
         }
       }

@@ -111,6 +111,10 @@ struct PdsArgs {
   float scale_log2;
   uint32_t* status;
   int64_t n_blocks = 0;  // blocks in p_out and ds_out
+  uint64_t wait_limit_ns = kLaunchWaitLimitNs;
+  // failure-path self-test only (-1 otherwise): the K/V ring unit with this index is
+  // never loaded, so the wait for it runs out after wait_limit_ns
+  int test_skip_unit = -1;
 };
 // Both blocks of every (query tile, key tile) pair in one pass: P = exp(S - LSE)
 // into a.p_out and dS = P (dP - Delta) into a.ds_out.

@@ -397,7 +397,8 @@ def dualkv_selftest_kernel(which: int, limit_ns: int, stream=None) -> None:
     """Runs a production kernel on a tiny internal layout with its failure path
     forced (0: forward, a K/V tile never loaded; 1: dK/dV, a query block one
     barrier arrival short; 2: forward, a work item past the last row; 3: dQ, a
-    work item past the last row) and every wait limited to limit_ns.  dualkv_check_status() then raises DUALKV_ERR_DEVICE."""
+    work item past the last row; 4: the D = 512 P / dS pass, a K/V tile never
+    loaded) and every wait limited to limit_ns.  dualkv_check_status() then raises DUALKV_ERR_DEVICE."""
     _raise(load().dualkv_selftest_kernel(int(which), int(limit_ns), _stream(stream)), "dualkv_selftest_kernel")
 
 

@@ -36,10 +36,12 @@ KERNEL_CASES = [
     (1, "dK/dV: a query block one barrier arrival short"),
     (2, "forward: a work item past the last row"),
     (3, "dQ: a work item past the last row, emptied by the preprocess"),
+    (4, "D = 512 P / dS pass: a K/V tile never loaded"),
 ]
 
 
-@pytest.mark.parametrize("which,what", KERNEL_CASES, ids=["fwd-timeout", "dkv-timeout", "fwd-bounds", "dq-bounds"])
+@pytest.mark.parametrize("which,what", KERNEL_CASES,
+                         ids=["fwd-timeout", "dkv-timeout", "fwd-bounds", "dq-bounds", "pds512-timeout"])
 def test_production_kernel_failure_paths(which, what):
     # the real kernels' failure handling: the bounded waits (50 ms here) run out, or
     # the range check skips the bad entry; the kernel drains, frees its tensor memory

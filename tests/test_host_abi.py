@@ -151,7 +151,7 @@ def test_selftest_rejects_out_of_range_limit(lib):
     assert lib.dualkv_selftest_timeout(10, None) == dualkv.DUALKV_ERR_INVALID
     assert lib.dualkv_selftest_timeout(100 * 10**9, None) == dualkv.DUALKV_ERR_INVALID
     assert lib.dualkv_selftest_kernel(0, 10, None) == dualkv.DUALKV_ERR_INVALID
-    assert lib.dualkv_selftest_kernel(4, 50_000_000, None) == dualkv.DUALKV_ERR_INVALID
+    assert lib.dualkv_selftest_kernel(5, 50_000_000, None) == dualkv.DUALKV_ERR_INVALID
     assert lib.dualkv_selftest_kernel(-1, 50_000_000, None) == dualkv.DUALKV_ERR_INVALID
 
 
