@@ -56,10 +56,11 @@ constexpr int kPdsThreads = 320;
 struct PdsFCfg {
   static constexpr int BM = 128, BN = 128;
   static constexpr int QCH = kD / 64;              // 64-column chunks of Q / dO / K / V
-  static constexpr int UNIT_BYTES = 2 * BN * 128;  // two 64-column chunks of a key tile
-  static constexpr int KU = QCH / 2;               // units per K or V tile
+  static constexpr int UCH = 2;                    // 64-column chunks of a key tile per ring unit
+  static constexpr int UNIT_BYTES = UCH * BN * 128;
+  static constexpr int KU = QCH / UCH;             // units per K or V tile
   static constexpr int A_BYTES = BM * kD * 2;      // 128 KB: dO resident (Q staged here first)
-  static constexpr int NST = 3;
+  static constexpr int NST = 6 / UCH;              // 96 KB of ring
   static constexpr int OFF_A = 0, OFF_RING = A_BYTES;
   static constexpr int SMEM_BYTES = OFF_RING + NST * UNIT_BYTES + 1024;
   static constexpr uint32_t TM_S = 0, TM_DP = BN, TM_Q = 2 * BN, TM_COLS = 512;
@@ -67,7 +68,7 @@ struct PdsFCfg {
 
 struct PdsFCtl {
   uint64_t q_full, q_tmem, do_full;
-  uint64_t ring_full[3], ring_empty[3];
+  uint64_t ring_full[6], ring_empty[6];
   uint64_t s_full, s_empty, dp_full, dp_empty;
   uint64_t drain;
   uint32_t tmem_base;
@@ -142,8 +143,8 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
             if (idx == a.test_skip_unit) continue;  // failure-path self-test: never loaded
             mbar_arrive_expect_tx(&ctl.ring_full[slot], C::UNIT_BYTES);
             uint8_t* dst = sRing + slot * C::UNIT_BYTES;
-            for (int c = 0; c < 2; ++c)
-              tma_load_3d(dst + c * C::BN * 128, tm, &ctl.ring_full[slot], (2 * u + c) * 64, kvh, key_row);
+            for (int c = 0; c < C::UCH; ++c)
+              tma_load_3d(dst + c * C::BN * 128, tm, &ctl.ring_full[slot], (C::UCH * u + c) * 64, kvh, key_row);
           }
           if (j == 0 && kind == 0 && ok) {
             // dO replaces the staged Q once the compute warps have copied Q into TMEM
@@ -190,10 +191,10 @@ __global__ void __launch_bounds__(kPdsThreads, 1)
             const uint64_t bdesc = sdesc_sw128(aRing + slot * C::UNIT_BYTES, 16, 1024);
             if (elect_one()) {
 #pragma unroll
-              for (int c = 0; c < 2; ++c)
+              for (int c = 0; c < C::UCH; ++c)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                  const int kc = 2 * u + c;  // 64-column chunk of the contraction
+                  const int kc = C::UCH * u + c;  // 64-column chunk of the contraction
                   if (kind == 0)
                     mma_bf16_ts(tD, tmem + C::TM_Q + 8 * (kc * 4 + k), sdesc_add(bdesc, c * C::BN * 128 + k * 32),
                                 idS, (u | c | k) != 0);
